@@ -1,0 +1,146 @@
+"""CPU oracle for query-aware sparse decode: ctypes wrapper over quest_oracle.c.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's
+CPU-baseline leg are the only callers; the product path (the CUDA library and
+its Python binding) never imports this package.
+
+Functions take numpy arrays (bf16 data as uint16 bit patterns) and return
+numpy arrays.  See quest_oracle.c for what each one computes and which
+passage it follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "quest_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "libquest_oracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-fno-fast-math", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        P = ctypes.c_void_p
+        i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
+        lib.oracle_update_meta.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, i64]
+        lib.oracle_select.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, P, P, P]
+        lib.oracle_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, f32, P, P]
+        for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode):
+            f.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: Optional[np.ndarray]):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    assert a.dtype == dtype, (a.dtype, dtype)
+    return a
+
+
+class Cache:
+    """Host copy of a paged pool: k/v [n_phys][Hkv][P][D] and meta [n_phys][Hkv][2][D]."""
+
+    def __init__(self, n_phys: int, num_kv_heads: int, page_size: int = 16, head_dim: int = 128,
+                 fill_bits: int = 0):
+        shape = (n_phys, num_kv_heads, page_size, head_dim)
+        self.k = np.full(shape, fill_bits, dtype=np.uint16)
+        self.v = np.full(shape, fill_bits, dtype=np.uint16)
+        self.meta = np.zeros((n_phys, num_kv_heads, 2, head_dim), dtype=np.uint16)
+        self.n_phys, self.Hkv, self.P, self.D = n_phys, num_kv_heads, page_size, head_dim
+
+
+def update_meta(cache: Cache, k_new: np.ndarray, v_new: np.ndarray, slot_mapping: np.ndarray) -> None:
+    k_new = _c(k_new, np.uint16)
+    v_new = _c(v_new, np.uint16)
+    slot_mapping = _c(slot_mapping, np.int32)
+    T = slot_mapping.shape[0]
+    assert k_new.shape == (T, cache.Hkv, cache.D) and v_new.shape == k_new.shape
+    rc = _load().oracle_update_meta(_ptr(cache.k), _ptr(cache.v), _ptr(cache.meta), cache.n_phys,
+                                    cache.Hkv, cache.P, cache.D, _ptr(k_new), _ptr(v_new),
+                                    _ptr(slot_mapping), T)
+    if rc != 0:
+        raise ValueError(f"oracle_update_meta failed ({rc})")
+
+
+def select(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
+           budget_pages: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Returns (sel_idx [B][Hkv][K] int32, sel_cnt [B][Hkv] int32, scores [B][Hkv][max_pages] fp32).
+
+    Score entries past a request's last page are NaN."""
+    q = _c(q, np.uint16)
+    page_table = _c(page_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    max_pages = page_table.shape[1]
+    K = int(budget_pages)
+    sel_idx = np.empty((B, cache.Hkv, K), dtype=np.int32)
+    sel_cnt = np.empty((B, cache.Hkv), dtype=np.int32)
+    scores = np.full((B, cache.Hkv, max_pages), np.nan, dtype=np.float32)
+    rc = _load().oracle_select(_ptr(q), _ptr(cache.meta), _ptr(page_table), _ptr(seq_lens), B, Hq,
+                               cache.Hkv, D, cache.P, max_pages, K, cache.n_phys, _ptr(sel_idx),
+                               _ptr(sel_cnt), _ptr(scores))
+    if rc != 0:
+        raise ValueError(f"oracle_select failed ({rc})")
+    return sel_idx, sel_cnt, scores
+
+
+def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
+           sel_idx: Optional[np.ndarray] = None, sel_cnt: Optional[np.ndarray] = None,
+           scale: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
+    """Returns (out fp32 [B][Hq][D], lse fp32 [B][Hq]); dense when sel_idx is None."""
+    q = _c(q, np.uint16)
+    page_table = _c(page_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    max_pages = page_table.shape[1]
+    if scale is None:
+        scale = 1.0 / float(np.sqrt(D))
+    K = 0
+    if sel_idx is not None:
+        sel_idx = _c(sel_idx, np.int32)
+        sel_cnt = _c(sel_cnt, np.int32)
+        K = sel_idx.shape[2]
+    out = np.empty((B, Hq, D), dtype=np.float32)
+    lse = np.empty((B, Hq), dtype=np.float32)
+    rc = _load().oracle_decode(_ptr(q), _ptr(cache.k), _ptr(cache.v), _ptr(page_table), _ptr(seq_lens),
+                               B, Hq, cache.Hkv, D, cache.P, max_pages, cache.n_phys, _ptr(sel_idx),
+                               _ptr(sel_cnt), K, float(scale), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError(f"oracle_decode failed ({rc})")
+    return out, lse
+
+
+def build_cache(wl, fill_bits: int) -> Cache:
+    """Pool + metadata after a workload's whole prefill, appended in 4096-token chunks.
+
+    `wl` is a synthetic workload (token stream, slot mapping, pool size);
+    `fill_bits` is the bf16 pattern of pool slots that never receive a token."""
+    s = wl.spec
+    cache = Cache(wl.num_phys_pages, s.num_kv_heads, s.page_size, s.head_dim, fill_bits)
+    for a, b in wl.prefill_chunks():
+        update_meta(cache, wl.k_tok[a:b], wl.v_tok[a:b], wl.slot_mapping[a:b])
+    return cache

@@ -1,0 +1,257 @@
+/*
+ * CPU oracle for query-aware (Quest-style) sparse decode attention over a
+ * paged KV cache.  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and
+ * the benchmark's CPU-baseline leg are the only callers.  Nothing on the
+ * product path links or calls this file, and it shares no code with the CUDA
+ * library (its own bf16 helpers, its own loops).
+ *
+ * What it follows:
+ *  - "add-sparse-method" skill page, "Placement Rules" 3-4: metadata is
+ *    updated after KV is written (on_kv_stored), and the decode-time view is
+ *    built from the current layer's q (build_decode_view).
+ *  - SparseEngine summary page, section "method key points": Quest performs
+ *    query-relevant page selection over per-method cache metadata, and the
+ *    attention backend consumes the resulting view.
+ *  - The method statement these pages leave open is fixed as follows: each
+ *    page stores the per-channel min and max of its keys; a page's score is
+ *    the upper bound sum_i max(q_i*kmax_i, q_i*kmin_i), summed over the query
+ *    heads of one kv group; each (request, kv head) keeps its top-K pages,
+ *    ties going to the lower page index; exact softmax attention runs over
+ *    only those pages.
+ *
+ * It is written literally: the score uses the max-form above (not any
+ * rearrangement of it), ranking is a full sort, attention is two passes
+ * over an explicit score vector.  Accumulation is fp32 in the loop order
+ * written (heads, then channels; tokens in ascending page order).
+ *
+ * Layouts (bf16 values are passed as uint16 bit patterns):
+ *   k_pool, v_pool  [n_phys][Hkv][P][D]
+ *   meta            [n_phys][Hkv][2][D]   ([0] = kmin, [1] = kmax)
+ *   q               [B][Hq][D]            query head h belongs to kv group h / (Hq/Hkv)
+ *   page_table      [B][max_pages]        logical page -> physical page
+ *   seq_lens        [B]
+ *   sel_idx         [B][Hkv][K]           selected logical pages, ascending, -1 padded
+ *   sel_cnt         [B][Hkv]
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Exact when f already holds a bf16 value (its low 16 bits are zero). */
+static uint16_t float_to_bf16_bits_exact(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(u >> 16);
+}
+
+/*
+ * Append T tokens: copy each token's key and value row into its slot, then
+ * recompute, from scratch, the key min/max of every page this call touched,
+ * over that page's filled offsets [0, filled).  Pages fill in offset order
+ * without holes, so a page's fill after this call is one past the largest
+ * offset written to it here.
+ */
+int oracle_update_meta(uint16_t* k_pool, uint16_t* v_pool, uint16_t* meta,
+                       int64_t n_phys, int Hkv, int P, int D,
+                       const uint16_t* k_new, const uint16_t* v_new,
+                       const int32_t* slot_mapping, int64_t T) {
+    int32_t* fill = (int32_t*)calloc((size_t)n_phys, sizeof(int32_t));
+    if (!fill) return -1;
+    const size_t row = (size_t)D;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        int64_t page = slot / P;
+        int off = (int)(slot % P);
+        if (slot < 0 || page >= n_phys) { free(fill); return -2; }
+        for (int h = 0; h < Hkv; ++h) {
+            size_t dst = (((size_t)page * Hkv + h) * P + off) * row;
+            size_t src = ((size_t)t * Hkv + h) * row;
+            memcpy(k_pool + dst, k_new + src, row * sizeof(uint16_t));
+            memcpy(v_pool + dst, v_new + src, row * sizeof(uint16_t));
+        }
+        if (off + 1 > fill[page]) fill[page] = off + 1;
+    }
+    for (int64_t page = 0; page < n_phys; ++page) {
+        int filled = fill[page];
+        if (filled == 0) continue;
+        for (int h = 0; h < Hkv; ++h) {
+            uint16_t* mn = meta + (((size_t)page * Hkv + h) * 2 + 0) * row;
+            uint16_t* mx = meta + (((size_t)page * Hkv + h) * 2 + 1) * row;
+            for (int i = 0; i < D; ++i) {
+                float lo = INFINITY, hi = -INFINITY;
+                for (int o = 0; o < filled; ++o) {
+                    float k = bf16_bits_to_float(k_pool[(((size_t)page * Hkv + h) * P + o) * row + i]);
+                    if (k < lo) lo = k;
+                    if (k > hi) hi = k;
+                }
+                mn[i] = float_to_bf16_bits_exact(lo);
+                mx[i] = float_to_bf16_bits_exact(hi);
+            }
+        }
+    }
+    free(fill);
+    return 0;
+}
+
+/*
+ * Upper-bound score of one page for one kv group:
+ *   s = sum over query heads h of the group, sum over channels i, of
+ *       max(q[h][i] * kmax[i], q[h][i] * kmin[i]).
+ */
+static float page_bound(const uint16_t* q_group, int G, int D,
+                        const uint16_t* kmin, const uint16_t* kmax) {
+    float s = 0.0f;
+    for (int h = 0; h < G; ++h) {
+        for (int i = 0; i < D; ++i) {
+            float qi = bf16_bits_to_float(q_group[(size_t)h * D + i]);
+            float a = qi * bf16_bits_to_float(kmax[i]);
+            float c = qi * bf16_bits_to_float(kmin[i]);
+            s += (a > c) ? a : c;
+        }
+    }
+    return s;
+}
+
+typedef struct {
+    float score;
+    int32_t page;
+} scored_page;
+
+/* Higher score first; equal scores: lower logical page index first. */
+static int by_score_then_index(const void* pa, const void* pb) {
+    const scored_page* a = (const scored_page*)pa;
+    const scored_page* b = (const scored_page*)pb;
+    if (a->score > b->score) return -1;
+    if (a->score < b->score) return 1;
+    return (a->page < b->page) ? -1 : (a->page > b->page);
+}
+
+static int by_int_ascending(const void* pa, const void* pb) {
+    int32_t a = *(const int32_t*)pa, b = *(const int32_t*)pb;
+    return (a < b) ? -1 : (a > b);
+}
+
+/*
+ * For every request b and kv group g: score each of the request's
+ * n_b = ceil(len_b / P) logical pages, keep the min(K, n_b) best under the
+ * order (score desc, page asc), and emit their logical indices ascending.
+ * scores (nullable) receives [B][Hkv][max_pages] fp32, entries past n_b untouched.
+ */
+int oracle_select(const uint16_t* q, const uint16_t* meta,
+                  const int32_t* page_table, const int32_t* seq_lens,
+                  int B, int Hq, int Hkv, int D, int P, int max_pages, int K,
+                  int64_t n_phys, int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
+    if (Hq % Hkv != 0 || K < 1) return -1;
+    const int G = Hq / Hkv;
+    scored_page* list = (scored_page*)malloc((size_t)max_pages * sizeof(scored_page));
+    if (!list) return -1;
+    for (int b = 0; b < B; ++b) {
+        int n = (seq_lens[b] + P - 1) / P;
+        if (n < 1 || n > max_pages) { free(list); return -2; }
+        for (int g = 0; g < Hkv; ++g) {
+            const uint16_t* qg = q + ((size_t)b * Hq + (size_t)g * G) * D;
+            for (int p = 0; p < n; ++p) {
+                int64_t phys = page_table[(size_t)b * max_pages + p];
+                if (phys < 0 || phys >= n_phys) { free(list); return -2; }
+                const uint16_t* kmin = meta + (((size_t)phys * Hkv + g) * 2 + 0) * D;
+                const uint16_t* kmax = meta + (((size_t)phys * Hkv + g) * 2 + 1) * D;
+                list[p].score = page_bound(qg, G, D, kmin, kmax);
+                list[p].page = p;
+                if (scores) scores[((size_t)b * Hkv + g) * max_pages + p] = list[p].score;
+            }
+            qsort(list, (size_t)n, sizeof(scored_page), by_score_then_index);
+            int m = n < K ? n : K;
+            int32_t* out = sel_idx + ((size_t)b * Hkv + g) * K;
+            for (int j = 0; j < m; ++j) out[j] = list[j].page;
+            qsort(out, (size_t)m, sizeof(int32_t), by_int_ascending);
+            for (int j = m; j < K; ++j) out[j] = -1;
+            sel_cnt[(size_t)b * Hkv + g] = m;
+        }
+    }
+    free(list);
+    return 0;
+}
+
+/*
+ * Exact softmax attention of every query head over the tokens of a page
+ * list: all n_b logical pages when sel_idx is NULL (dense), else the
+ * sel_cnt[b][g] pages of sel_idx[b][g].  The last logical page n_b - 1 holds
+ * len_b - P*(n_b - 1) tokens; every other page holds P.
+ *   z_t = (q . k_t) * scale;  m = max z;  l = sum exp(z - m);
+ *   out = sum exp(z_t - m) v_t / l;  lse = m + ln(l).
+ * out is fp32 [B][Hq][D]; lse fp32 [B][Hq].
+ */
+int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                  const int32_t* page_table, const int32_t* seq_lens,
+                  int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
+                  const int32_t* sel_idx, const int32_t* sel_cnt, int K, float scale,
+                  float* out, float* lse) {
+    if (Hq % Hkv != 0) return -1;
+    const int G = Hq / Hkv;
+    float* z = (float*)malloc((size_t)max_pages * P * sizeof(float));
+    int32_t* tok_page = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
+    int32_t* tok_off = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
+    if (!z || !tok_page || !tok_off) { free(z); free(tok_page); free(tok_off); return -1; }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int len = seq_lens[b];
+        int n = (len + P - 1) / P;
+        if (n < 1 || n > max_pages) { rc = -2; break; }
+        for (int h = 0; h < Hq && rc == 0; ++h) {
+            int g = h / G;
+            int count = sel_idx ? sel_cnt[(size_t)b * Hkv + g] : n;
+            if (count < 0 || count > (sel_idx ? K : n)) { rc = -2; break; }
+            /* Gather the attended tokens as (physical page, offset). */
+            int ntok = 0;
+            for (int j = 0; j < count; ++j) {
+                int p = sel_idx ? sel_idx[((size_t)b * Hkv + g) * K + j] : j;
+                if (p < 0 || p >= n) { rc = -2; break; }
+                int64_t phys = page_table[(size_t)b * max_pages + p];
+                if (phys < 0 || phys >= n_phys) { rc = -2; break; }
+                int valid = (p == n - 1) ? len - P * (n - 1) : P;
+                for (int o = 0; o < valid; ++o) {
+                    tok_page[ntok] = (int32_t)phys;
+                    tok_off[ntok] = o;
+                    ++ntok;
+                }
+            }
+            if (rc) break;
+            const uint16_t* qh = q + ((size_t)b * Hq + h) * D;
+            float* o_row = out + ((size_t)b * Hq + h) * D;
+            float m = -INFINITY;
+            for (int t = 0; t < ntok; ++t) {
+                const uint16_t* k = k_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
+                float dot = 0.0f;
+                for (int i = 0; i < D; ++i) dot += bf16_bits_to_float(qh[i]) * bf16_bits_to_float(k[i]);
+                z[t] = dot * scale;
+                if (z[t] > m) m = z[t];
+            }
+            float l = 0.0f;
+            for (int i = 0; i < D; ++i) o_row[i] = 0.0f;
+            for (int t = 0; t < ntok; ++t) {
+                float w = expf(z[t] - m);
+                l += w;
+                const uint16_t* v = v_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
+                for (int i = 0; i < D; ++i) o_row[i] += w * bf16_bits_to_float(v[i]);
+            }
+            if (ntok == 0) {
+                lse[(size_t)b * Hq + h] = -INFINITY;
+                continue;
+            }
+            for (int i = 0; i < D; ++i) o_row[i] /= l;
+            lse[(size_t)b * Hq + h] = m + logf(l);
+        }
+    }
+    free(z);
+    free(tok_page);
+    free(tok_off);
+    return rc;
+}

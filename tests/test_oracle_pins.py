@@ -1,0 +1,325 @@
+"""Pins of the CPU oracle against what the method and the mathematics fix
+(no GPU).  Each test checks the oracle against something other than its own
+code: hand-worked values, the box-corner definition of the bound, closed
+forms, an invariant, brute-force subset search and torch's scaled-dot-product
+attention in fp64."""
+from __future__ import annotations
+
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from query_aware_sparse_quest_gb300 import synth
+from query_aware_sparse_quest_gb300.synth import bf16_bits_to_f32, to_bf16_bits
+
+from helpers import bf, box_bound_bruteforce, page_tokens, request_keys
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_example.txt")
+
+
+def _golden():
+    vals = {}
+    for line in open(GOLDEN):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        k, *v = line.split()
+        vals[k] = [float(x) for x in v]
+    return vals
+
+
+def _explicit_cache(pages, P, D, Hkv=1):
+    """Cache holding `pages` (list of [P][Hkv][D] key arrays) contiguously."""
+    n = len(pages)
+    cache = oracle.Cache(n, Hkv, P, D, fill_bits=0)
+    k = np.concatenate([bf(np.asarray(pg, dtype=np.float64).reshape(P, Hkv, D)) for pg in pages])
+    v = np.zeros_like(k)
+    oracle.update_meta(cache, k, v, np.arange(n * P, dtype=np.int32))
+    return cache
+
+
+# ---------------------------------------------------------------- worked example
+
+def test_worked_example_scores_and_ties():
+    g = _golden()
+    pages = [[[1, 3], [-1, 0]], [[2, 0], [0, 1]], [[1, -1], [0, -1]], [[2, 0], [0, 0]]]
+    cache = _explicit_cache(pages, P=2, D=2)
+    q = bf([[[1, -2]]])
+    pt = np.arange(4, dtype=np.int32)[None]
+    sl = np.array([8], dtype=np.int32)
+    idx2, cnt2, s = oracle.select(cache, q, pt, sl, 2)
+    assert s[0, 0].tolist() == g["caseA_scores"]
+    assert idx2[0, 0].tolist() == [int(x) for x in g["caseA_top2"]] and cnt2[0, 0] == 2
+    idx3, _, _ = oracle.select(cache, q, pt, sl, 3)
+    assert idx3[0, 0].tolist() == [int(x) for x in g["caseA_top3"]]
+    # metadata layout: [0] = kmin, [1] = kmax
+    meta0 = bf16_bits_to_f32(cache.meta[0, 0])
+    assert meta0[0].tolist() == [-1, 0] and meta0[1].tolist() == [1, 3]
+
+
+def test_worked_example_gqa_group_sum():
+    g = _golden()
+    cache = _explicit_cache([[[1, 3], [-1, 0]]], P=2, D=2)
+    q = bf([[[1, -2], [-0.5, 0.25]]])           # two query heads, one kv group
+    _, _, s = oracle.select(cache, q, np.zeros((1, 1), np.int32), np.array([2], np.int32), 1)
+    assert s[0, 0, 0] == g["caseB_score"][0]
+
+
+def test_worked_example_attention():
+    g = _golden()
+    cache = oracle.Cache(1, 1, 2, 2, fill_bits=0)
+    oracle.update_meta(cache, bf([[[1, 3]], [[-1, 0]]]), bf([[[2, 0]], [[0, 4]]]),
+                       np.array([0, 1], np.int32))
+    out, lse = oracle.decode(cache, bf([[[1, -2]]]), np.zeros((1, 1), np.int32),
+                             np.array([2], np.int32), scale=1.0)
+    np.testing.assert_allclose(out[0, 0], g["caseC_out"], rtol=1e-6)
+    np.testing.assert_allclose(lse[0, 0], g["caseC_lse"][0], rtol=1e-6)
+
+
+# ---------------------------------------------------------------- bound definition
+
+def _tiny_spec(**kw):
+    base = dict(name="tiny", batch=2, num_q_heads=4, num_kv_heads=2, ctx=45, budget_pages=3,
+                seed=11, head_dim=4, page_size=4, shuffle_pool=True)
+    base.update(kw)
+    return synth.Spec(**base)
+
+
+@pytest.mark.parametrize("D,P,Hq,Hkv,ctx,outlier", [
+    (1, 3, 1, 1, 10, False),
+    (3, 4, 4, 2, 45, True),
+    (5, 2, 3, 1, 9, False),
+    (6, 5, 6, 3, 23, True),
+])
+def test_bound_equals_box_corner_maximum(D, P, Hq, Hkv, ctx, outlier):
+    """The score of a page equals, per query head, the maximum of q.x over all
+    2^D corners of the page's per-channel key box, summed over the group."""
+    wl = synth.make_workload(_tiny_spec(head_dim=D, page_size=P, num_q_heads=Hq, num_kv_heads=Hkv,
+                                        ctx=ctx, outlier_channels=outlier, seed=D * 7 + P))
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    _, _, scores = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, 2)
+    G = Hq // Hkv
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    for b in range(wl.spec.batch):
+        k, _ = request_keys(wl, b)
+        n = -(-int(wl.seq_lens[b]) // P)
+        for p in range(n):
+            toks = slice(p * P, min(int(wl.seq_lens[b]), (p + 1) * P))
+            for g in range(Hkv):
+                want = box_bound_bruteforce(qf[b, g * G : (g + 1) * G], k[toks, g])
+                np.testing.assert_allclose(scores[b, g, p], want, rtol=2e-6, atol=1e-6)
+
+
+@pytest.mark.parametrize("cfg", [0, 1])
+def test_bound_dominates_true_max(cfg):
+    """Invariant: for every page and kv group, the bound is at least the sum
+    over the group's heads of each head's largest q.k on that page (fp64)."""
+    spec = synth.SPECS[cfg]
+    if cfg == 1:
+        spec = spec.scaled(batch=2, ctx=1000)
+    wl = synth.make_workload(spec)
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    _, _, scores = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, spec.budget_pages)
+    P, Hkv = spec.page_size, spec.num_kv_heads
+    G = spec.num_q_heads // Hkv
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    for b in range(spec.batch):
+        k, _ = request_keys(wl, b)
+        L = int(wl.seq_lens[b])
+        n = -(-L // P)
+        for g in range(Hkv):
+            logits = np.einsum("hd,td->ht", qf[b, g * G : (g + 1) * G], k[:, g])   # [G][L]
+            pad = n * P - L
+            lp = np.pad(logits, ((0, 0), (0, pad)), constant_values=-np.inf).reshape(G, n, P)
+            true_max_group = lp.max(axis=2).sum(axis=0)                              # [n]
+            s = scores[b, g, :n].astype(np.float64)
+            assert np.all(s >= true_max_group - 1e-5 * np.abs(s) - 1e-4)
+
+
+def test_bound_closed_forms():
+    """One-token page: bound = sum_h q_h.k.  Identical keys: bound = sum_h q_h.k.
+    All q >= 0: bound = sum_h q_h.kmax.  All q <= 0: bound = sum_h q_h.kmin."""
+    rng = np.random.default_rng(5)
+    D, P = 8, 4
+    keys = to_bf16_bits(rng.standard_normal((3, P, 1, D)).astype(np.float32))
+    keys[1] = keys[1][0:1]                 # page 1: four identical keys
+    kf = bf16_bits_to_f32(keys).astype(np.float64)
+    cache = oracle.Cache(3, 1, P, D, fill_bits=0)
+    T = 2 * P + 1                          # page 2 holds a single token
+    oracle.update_meta(cache, keys.reshape(-1, 1, D)[:T], keys.reshape(-1, 1, D)[:T],
+                       np.arange(T, dtype=np.int32))
+    pt = np.arange(3, dtype=np.int32)[None]
+    sl = np.array([T], np.int32)
+    qmix = to_bf16_bits(rng.standard_normal((1, 2, D)).astype(np.float32))
+    qpos = to_bf16_bits(np.abs(rng.standard_normal((1, 2, D))).astype(np.float32))
+    qneg = to_bf16_bits(-np.abs(rng.standard_normal((1, 2, D))).astype(np.float32))
+    for q in (qmix, qpos, qneg):
+        qf = bf16_bits_to_f32(q).astype(np.float64)[0]
+        _, _, s = oracle.select(cache, q, pt, sl, 1)
+        np.testing.assert_allclose(s[0, 0, 2], (qf @ kf[2, 0, 0]).sum(), rtol=1e-6)
+        np.testing.assert_allclose(s[0, 0, 1], (qf @ kf[1, 0, 0]).sum(), rtol=1e-6)
+    kmax, kmin = kf[0, :, 0].max(axis=0), kf[0, :, 0].min(axis=0)
+    _, _, s = oracle.select(cache, qpos, pt, sl, 1)
+    np.testing.assert_allclose(s[0, 0, 0], (bf16_bits_to_f32(qpos)[0] @ kmax).sum(), rtol=1e-6)
+    _, _, s = oracle.select(cache, qneg, pt, sl, 1)
+    np.testing.assert_allclose(s[0, 0, 0], (bf16_bits_to_f32(qneg)[0] @ kmin).sum(), rtol=1e-6)
+
+
+# ---------------------------------------------------------------- ranking
+
+@pytest.mark.parametrize("seed", range(12))
+def test_ranking_matches_bruteforce_subsets(seed):
+    """Tiny integer-valued inputs (exact scores, many exact ties): the selected
+    set maximises the sum of page scores over all K-subsets, and among the
+    maximisers it is the lexicographically smallest index set."""
+    rng = np.random.default_rng(100 + seed)
+    D, P = int(rng.integers(1, 5)), int(rng.integers(1, 4))
+    Hkv, G = 1, int(rng.integers(1, 3))
+    n = int(rng.integers(1, 11))
+    L = (n - 1) * P + int(rng.integers(1, P + 1))
+    K = int(rng.integers(1, n + 2))
+    k = bf(rng.integers(-3, 4, size=(L, Hkv, D)).astype(np.float64))
+    q = bf(rng.integers(-2, 3, size=(1, G * Hkv, D)).astype(np.float64))
+    phys = rng.permutation(n).astype(np.int32)
+    cache = oracle.Cache(n, Hkv, P, D, fill_bits=0)
+    pos = np.arange(L)
+    oracle.update_meta(cache, k, k, (phys[pos // P] * P + pos % P).astype(np.int32))
+    sel, cnt, _ = oracle.select(cache, q, phys[None], np.array([L], np.int32), K)
+    kf = bf16_bits_to_f32(k).astype(np.float64)
+    qf = bf16_bits_to_f32(q).astype(np.float64)[0]
+    s = [box_bound_bruteforce(qf, kf[p * P : min(L, (p + 1) * P), 0]) for p in range(n)]
+    m = min(K, n)
+    best = max(itertools.combinations(range(n), m),
+               key=lambda c: (sum(s[i] for i in c), [-i for i in c]))
+    assert cnt[0, 0] == m
+    assert sel[0, 0, :m].tolist() == list(best)
+    assert sel[0, 0, m:].tolist() == [-1] * (K - m)
+
+
+# ---------------------------------------------------------------- attention
+
+def _sdpa_fp64(q_heads, k, v, scale):
+    """torch's scaled_dot_product_attention (fp64, CPU) of heads [H][D] over tokens [T][D]."""
+    qt = torch.from_numpy(q_heads)[None, :, None, :]           # [1][H][1][D]
+    kt = torch.from_numpy(k)[None, None].expand(1, q_heads.shape[0], -1, -1)
+    vt = torch.from_numpy(v)[None, None].expand(1, q_heads.shape[0], -1, -1)
+    o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, scale=scale)
+    z = (torch.from_numpy(q_heads) @ torch.from_numpy(k).T) * scale
+    return o[0, :, 0].numpy(), torch.logsumexp(z, dim=1).numpy()
+
+
+@pytest.mark.parametrize("cfg,ctx,batch", [(0, 4096, 1), (0, 1000, 1), (1, 777, 2), (3, 0, 3)])
+def test_dense_and_full_budget_match_sdpa(cfg, ctx, batch):
+    """(a) With K >= n every page is selected and sparse attention equals dense
+    attention; both equal fp64 softmax attention (torch SDPA) over the request's
+    valid tokens, and lse equals the log-sum-exp of the scaled logits."""
+    spec = synth.SPECS[cfg]
+    if cfg == 3:
+        spec = spec.scaled(batch=batch, ragged=(50, 600))
+    else:
+        spec = spec.scaled(batch=batch, ctx=ctx)
+    wl = synth.make_workload(spec)
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    n_pages = -(-wl.seq_lens // spec.page_size)
+    K = int(n_pages.max()) + 3
+    sel, cnt, _ = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, K)
+    for b in range(spec.batch):
+        assert cnt[b].tolist() == [n_pages[b]] * spec.num_kv_heads
+        assert sel[b, :, : n_pages[b]].tolist() == [list(range(n_pages[b]))] * spec.num_kv_heads
+    out_s, lse_s = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, sel, cnt)
+    out_d, lse_d = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens)
+    assert np.array_equal(out_s, out_d) and np.array_equal(lse_s, lse_d)
+    scale = 1.0 / np.sqrt(spec.head_dim)
+    G = spec.num_q_heads // spec.num_kv_heads
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    for b in range(spec.batch):
+        k, v = request_keys(wl, b)
+        for g in range(spec.num_kv_heads):
+            o_ref, l_ref = _sdpa_fp64(qf[b, g * G : (g + 1) * G], k[:, g], v[:, g], scale)
+            np.testing.assert_allclose(out_d[b, g * G : (g + 1) * G], o_ref, atol=2e-5, rtol=1e-4)
+            np.testing.assert_allclose(lse_d[b, g * G : (g + 1) * G], l_ref, atol=1e-5, rtol=1e-6)
+
+
+def test_sparse_attention_over_page_subset_matches_sdpa():
+    """Sparse attention equals fp64 softmax attention over exactly the tokens of
+    the listed pages, including a partial last page (its unfilled slots hold
+    large values that must not leak in)."""
+    spec = synth.SPECS[1].scaled(batch=2, ctx=16 * 37 + 5, budget_pages=9)
+    wl = synth.make_workload(spec)
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    rng = np.random.default_rng(3)
+    n = 38
+    Hkv, G, P = spec.num_kv_heads, spec.num_q_heads // spec.num_kv_heads, spec.page_size
+    sel = np.full((2, Hkv, 9), -1, np.int32)
+    cnt = np.zeros((2, Hkv), np.int32)
+    for b in range(2):
+        for g in range(Hkv):
+            m = int(rng.integers(1, 10))
+            pages = np.sort(rng.choice(n, size=m, replace=False))
+            if g == 0:
+                pages = np.unique(np.append(pages[: m - 1], n - 1))   # include the partial page
+            sel[b, g, : len(pages)] = pages
+            cnt[b, g] = len(pages)
+    out, lse = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, sel, cnt)
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    for b in range(2):
+        k, v = request_keys(wl, b)
+        for g in range(Hkv):
+            toks = np.concatenate([np.arange(p * P, min(int(wl.seq_lens[b]), (p + 1) * P))
+                                   for p in sel[b, g, : cnt[b, g]]])
+            o_ref, l_ref = _sdpa_fp64(qf[b, g * G : (g + 1) * G], k[toks, g], v[toks, g],
+                                      1.0 / np.sqrt(spec.head_dim))
+            np.testing.assert_allclose(out[b, g * G : (g + 1) * G], o_ref, atol=2e-5, rtol=1e-4)
+            np.testing.assert_allclose(lse[b, g * G : (g + 1) * G], l_ref, atol=1e-5)
+
+
+# ---------------------------------------------------------------- metadata
+
+@pytest.mark.parametrize("chunk", [1, 3, 16, 37])
+def test_update_meta_matches_page_min_max(chunk):
+    """After appends of `chunk` tokens per call, every page's metadata equals the
+    channel-wise min and max of the tokens appended to it (numpy reductions over
+    the token stream), the pool holds each token at its slot, and unfilled
+    slots are untouched."""
+    spec = synth.SPECS[3].scaled(batch=3, ragged=(20, 150), head_dim=8, seed=20 + chunk)
+    wl = synth.make_workload(spec)
+    P, Hkv = spec.page_size, spec.num_kv_heads
+    cache = oracle.Cache(wl.num_phys_pages, Hkv, P, spec.head_dim, fill_bits=synth.UNFILLED_BITS)
+    T = wl.k_tok.shape[0]
+    for a in range(0, T, chunk):
+        e = min(T, a + chunk)
+        oracle.update_meta(cache, wl.k_tok[a:e], wl.v_tok[a:e], wl.slot_mapping[a:e])
+    for b in range(spec.batch):
+        L = int(wl.seq_lens[b])
+        for p in range(-(-L // P)):
+            toks = page_tokens(wl, b, p)
+            phys = wl.page_table[b, p]
+            kf = bf16_bits_to_f32(wl.k_tok[toks]).astype(np.float64)      # [t][Hkv][D]
+            mf = bf16_bits_to_f32(cache.meta[phys]).astype(np.float64)    # [Hkv][2][D]
+            assert np.array_equal(mf[:, 0], kf.min(axis=0))
+            assert np.array_equal(mf[:, 1], kf.max(axis=0))
+            nv = len(toks)
+            assert np.array_equal(cache.k[phys, :, :nv].transpose(1, 0, 2), wl.k_tok[toks])
+            assert np.array_equal(cache.v[phys, :, :nv].transpose(1, 0, 2), wl.v_tok[toks])
+            assert np.all(cache.k[phys, :, nv:] == synth.UNFILLED_BITS)
+
+
+def test_needle_pages_rank_high():
+    """Sanity of the generator + bound (a statistic, not a parity claim): the
+    planted +8 sigma needle pages rank, on average, well inside the top quarter
+    of pages.  A single needle token does not always put its page in the top-K;
+    the bound sees only the part of the needle that leaves the page's key box."""
+    spec = synth.SPECS[2].scaled(batch=2, ctx=16000, needles_per_request=64)
+    wl = synth.make_workload(spec)
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    _, _, scores = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, spec.budget_pages)
+    pct = []
+    for b, p, _ in wl.needles:
+        for g in range(spec.num_kv_heads):
+            s = scores[b, g, :1000]
+            pct.append(float((s > s[p]).mean()))
+    assert np.mean(pct) < 0.25, np.mean(pct)
