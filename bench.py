@@ -1,0 +1,388 @@
+"""Benchmark: Quest sparse decode steps/s and achieved HBM bandwidth on one GB300.
+
+Workload: Qwen3-30B-A3B attention geometry (32 query / 4 kv heads, head_dim
+128), batch 8, 128000-token contexts in pages of 16 tokens (8000 pages per
+request), budget 4096 tokens (256 pages), 64 planted needle pages per request,
+physical pages shuffled over one pool; bf16 K/V/q, seeded synthetic data.
+
+A step is one attention layer's decode for the whole batch: page scoring,
+top-K selection and split-K attention over the selected pages
+(sv_quest_score + sv_quest_topk + sv_sparse_decode, the same kernels as
+sv_quest_select + sv_sparse_decode).  Inputs are resident in HBM; L2 is
+flushed before every timed step; each step is timed with CUDA events on the
+launching stream and the K step times are summed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas; weak scaling, no collective on the data path); rank 0 prints one
+JSON line with the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from query_aware_sparse_quest_gb300 import binding, build, resident, synth  # noqa: E402
+
+METRIC = "sparse-decode steps/s and achieved HBM GB/s vs ~8 TB/s at 128k ctx, batch 8"
+UNIT = "steps/s"
+BENCH_CONFIG = 2
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_pages_qwen3_b8_ctx128000.txt")
+KERNEL_SOURCES = {"score_pages_kernel": "query_aware_sparse_quest_gb300/csrc/svq_select.cu",
+                  "flash_decode_split_kernel": "query_aware_sparse_quest_gb300/csrc/svq_decode.cu"}
+
+
+# ---------------------------------------------------------------- helpers
+
+def dist_info():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms in the background."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(device_index), "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    vals = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if vals.get(f"{kernel}.source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals[f"{kernel}.dram_bytes_per_launch_full_size"])
+    except (KeyError, ValueError):
+        return None
+
+
+def algorithmic_bytes(wl):
+    """Per-step bytes the method must move (metadata + selected K/V + page tables + q/out),
+    and per-kernel figures for the roofline."""
+    s = wl.spec
+    P, Hkv, Hq, D = s.page_size, s.num_kv_heads, s.num_q_heads, s.head_dim
+    n = (wl.seq_lens.astype(np.int64) + P - 1) // P
+    sel = np.minimum(n, s.budget_pages)
+    meta = int(n.sum()) * Hkv * 2 * D * 2
+    pt = int(n.sum()) * 4
+    q = s.batch * Hq * D * 2
+    scores_w = int(n.sum()) * Hkv * 4
+    kv = int(sel.sum()) * Hkv * P * D * 2 * 2
+    sel_rd = int(sel.sum()) * Hkv * 4 * 2          # sel_idx + page-table entry per selected page
+    out = s.batch * Hq * D * 2 + s.batch * Hq * 4
+    dense_kv = int(n.sum()) * Hkv * P * D * 2 * 2
+    return {
+        "step": meta + kv + pt + q + out,
+        "score_pages_kernel": meta + pt + q + scores_w,
+        "flash_decode_split_kernel": kv + sel_rd + q,
+        "dense_step": dense_kv + pt + q + out,
+    }
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    rank, world, local_rank = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    build.build()
+
+    spec = synth.SPECS[BENCH_CONFIG]
+    wl = synth.make_workload(spec)
+    dw = resident.upload(wl, device=dev)
+    B, Hq, D = dw.q.shape
+    Hkv = spec.num_kv_heads
+    K = spec.budget_pages
+    max_pages = wl.max_pages
+    stream = torch.cuda.current_stream(dev)
+
+    scores = torch.empty((B, Hkv, max_pages), dtype=torch.float32, device=dev)
+    sel_idx, sel_cnt = resident.select_buffers(B, Hkv, K, dev)
+    ws = resident.workspace(binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, K), dev)
+    ws_dense = resident.workspace(binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, max_pages), dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step(q=None, page_table=None, seq_lens=None):
+        q = dw.q if q is None else q
+        pt = dw.page_table if page_table is None else page_table
+        sl = dw.seq_lens if seq_lens is None else seq_lens
+        binding.sv_quest_score(dw.cache, q, pt, sl, scores, stream)
+        ev[1].record(stream)
+        binding.sv_quest_topk(scores, sl, K, sel_idx, sel_cnt, stream)
+        ev[2].record(stream)
+        binding.sv_sparse_decode(dw.cache, q, pt, sl, sel_idx, sel_cnt, out, lse, ws, stream=stream)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    for _ in range(args.warmup):
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+
+    # ---- timed region: K steps, L2 flushed before each, device time summed
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.25)
+    t_score = t_topk = t_dec = 0.0
+    torch.cuda.synchronize(dev)
+    for _ in range(args.steps):
+        flush.zero_()
+        ev[0].record(stream)
+        step()
+        ev[3].record(stream)
+        ev[3].synchronize()
+        t_score += ev[0].elapsed_time(ev[1])
+        t_topk += ev[1].elapsed_time(ev[2])
+        t_dec += ev[2].elapsed_time(ev[3])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    total_ms = t_score + t_topk + t_dec
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+
+    # ---- dense (all pages) comparator, same flush discipline
+    n_dense = max(3, min(args.steps, 50))
+    t_dense = 0.0
+    for i in range(n_dense + 3):
+        flush.zero_()
+        ev[0].record(stream)
+        binding.sv_sparse_decode(dw.cache, dw.q, dw.page_table, dw.seq_lens, None, None, out, lse, ws_dense,
+                                 stream=stream)
+        ev[3].record(stream)
+        ev[3].synchronize()
+        if i >= 3:
+            t_dense += ev[0].elapsed_time(ev[3])
+    dense_ms = t_dense / n_dense
+
+    # ---- end to end through the public API: pinned host inputs in, results out
+    q_h = dw.q.cpu().pin_memory()
+    pt_h = dw.page_table.cpu().pin_memory()
+    sl_h = dw.seq_lens.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_d, pt_d, sl_d = torch.empty_like(dw.q), torch.empty_like(dw.page_table), torch.empty_like(dw.seq_lens)
+    n_e2e = max(3, min(args.steps, 200))
+    t_e2e = 0.0
+    for i in range(n_e2e + 3):
+        flush.zero_()
+        ev[0].record(stream)
+        q_d.copy_(q_h, non_blocking=True)
+        pt_d.copy_(pt_h, non_blocking=True)
+        sl_d.copy_(sl_h, non_blocking=True)
+        step(q_d, pt_d, sl_d)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        ev[3].record(stream)
+        ev[3].synchronize()
+        if i >= 3:
+            t_e2e += ev[0].elapsed_time(ev[3])
+    e2e_ms = t_e2e / n_e2e
+    h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    torch.cuda.synchronize(dev)
+    flags = binding.sv_get_device_error(reset=True)
+    if flags:
+        raise SystemExit(f"device error word {flags:#x}")
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+
+    ab = algorithmic_bytes(wl)
+    peak, peak_kind = measured_peaks()
+    per_kernel = {"score_pages_kernel": t_score / args.steps, "flash_decode_split_kernel": t_dec / args.steps}
+    dominant = max(per_kernel, key=per_kernel.get)
+    dom_ms = per_kernel[dominant]
+    if dominant == "flash_decode_split_kernel":
+        dom_note = "sv_sparse_decode time includes the small lse_combine kernel"
+    else:
+        dom_note = "sv_quest_score: one launch of score_pages_kernel"
+    achieved = ab[dominant] / (dom_ms * 1e-3) / 1e9
+    step_gbs = ab["step"] / (ms_per_step * 1e-3) / 1e9
+    value = world * 1e3 / ms_per_step
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": spec.name, "batch": B, "ctx_tokens": int(wl.seq_lens[0]), "page_size": spec.page_size,
+                   "budget_tokens": K * spec.page_size, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
+                   "needle_pages_per_request": spec.needles_per_request, "pool": "shuffled",
+                   "l2": "flushed before every timed step", "parallelism": f"replicas x{world}"},
+        "step_bytes": ab["step"],
+        "step_gbs": round(step_gbs, 1),
+        "step_roofline_frac": round(step_gbs / peak, 4),
+        "per_kernel_ms": {"score_pages": round(t_score / args.steps, 5), "topk_pages": round(t_topk / args.steps, 5),
+                          "sparse_decode(split+combine)": round(t_dec / args.steps, 5)},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "algorithmic_bytes": ab[dominant],
+                     "traffic": kernel_traffic(dominant), "note": dom_note},
+        "dense": {"steps_per_s": round(1e3 / dense_ms, 2), "ms_per_step": round(dense_ms, 5),
+                  "gbs": round(ab["dense_step"] / (dense_ms * 1e-3) / 1e9, 1), "bytes": ab["dense_step"]},
+        "e2e": {"value": round(world * 1e3 / e2e_ms, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        res["cpu_baseline"] = cpu_baseline(wl, max_seconds=args.cpu_seconds)
+    return res
+
+
+# ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
+
+def _oracle_host(wl):
+    import oracle
+    oracle.build()
+    return oracle, oracle.build_cache(wl, synth.UNFILLED_BITS)
+
+
+def _oracle_request_step(oracle, host, wl, b):
+    sl = slice(b, b + 1)
+    sel, cnt, _ = oracle.select(host, wl.q[sl], wl.page_table[sl], wl.seq_lens[sl], wl.spec.budget_pages)
+    oracle.decode(host, wl.q[sl], wl.page_table[sl], wl.seq_lens[sl], sel, cnt)
+
+
+def cpu_baseline(wl, max_seconds=10.0):
+    """The oracle as it stands (single thread, C, fp32), timed on this host over
+    whole requests of the same workload; value scaled to steps of the full batch."""
+    oracle, host = _oracle_host(wl)
+    B = wl.spec.batch
+    t0 = time.perf_counter()
+    done = 0
+    while done < 8 * B and (done < 1 or time.perf_counter() - t0 < max_seconds):
+        _oracle_request_step(oracle, host, wl, done % B)
+        done += 1
+    dt = time.perf_counter() - t0
+    per_step = dt / done * B
+    return {"value": round(1.0 / per_step, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{done} request(s) of the batch-{B} step (select + sparse decode), "
+                      f"{dt:.1f} s; value = 1 / (mean time per request x {B})"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return None
+    spec = synth.SPECS[BENCH_CONFIG]
+    wl = synth.make_workload(spec)
+    oracle, host = _oracle_host(wl)
+    B = spec.batch
+    for i in range(args.warmup):
+        _oracle_request_step(oracle, host, wl, i % B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        _oracle_request_step(oracle, host, wl, i % B)
+    dt = time.perf_counter() - t0
+    per_step = dt / args.steps * B
+    value = 1.0 / per_step
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_step * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": spec.name, "batch": B, "ctx_tokens": int(wl.seq_lens[0]), "page_size": spec.page_size,
+                   "budget_tokens": spec.budget_pages * spec.page_size, "num_q_heads": spec.num_q_heads,
+                   "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"each step = one request of the batch-{B} step (select + sparse decode); "
+                                   f"value = 1 / (mean time per request x {B})"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
+    res = run_reference(args) if args.impl == "reference" else run_gpu(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

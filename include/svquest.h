@@ -1,0 +1,169 @@
+/*
+ * svquest.h -- C ABI of libsvquest.so: query-aware (Quest-style) sparse decode
+ * attention over a paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * The three calls map the cache-manager hooks of the "add-sparse-method"
+ * skill page (section "Placement Rules", items 3-5) and the SparseEngine
+ * summary page (section "method key points": CacheManager, AttentionView):
+ *   on_kv_stored(...)      -> sv_quest_update_meta  (store K/V, refresh page metadata)
+ *   build_decode_view(q)   -> sv_quest_select       (query-aware page selection)
+ *   generic attention      -> sv_sparse_decode      (attention over the view)
+ *
+ * Conventions common to every call
+ *  - Every buffer argument is a DEVICE pointer, allocated and owned by the
+ *    caller; the library never allocates, frees or retains it.
+ *  - bf16 means IEEE bfloat16 stored as 16-bit words.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls enqueue kernels and return; they never synchronise.
+ *  - Arguments are checked on the host before anything is launched.  A
+ *    failed check returns a nonzero sv_status and launches nothing.  Values
+ *    that live on the device (page tables, slot mappings, selected indices)
+ *    cannot be checked on the host: kernels bounds-check them, skip any
+ *    access they would make out of range and record the fault in a device
+ *    error word read by sv_get_device_error().
+ *  - Geometry: page_size must be 16 and head_dim 128 (SV_ERR_UNSUPPORTED
+ *    otherwise); num_q_heads must be a multiple of num_kv_heads with at most
+ *    8 query heads per kv head; query head h reads kv head h / (Hq / Hkv).
+ *
+ * Layouts (row-major, innermost last)
+ *   k_pool, v_pool  bf16 [num_phys_pages][num_kv_heads][16][128]
+ *   meta            bf16 [num_phys_pages][num_kv_heads][2][128]
+ *                        [..][0][:] = per-channel key minimum of the page,
+ *                        [..][1][:] = per-channel key maximum
+ *   q               bf16 [B][num_q_heads][128]
+ *   page_table      int32 [B][max_pages]   logical page -> physical page
+ *   seq_lens        int32 [B]              tokens of each request, >= 1;
+ *                        request b has n_b = ceil(seq_lens[b] / 16) pages,
+ *                        the last holding seq_lens[b] - 16 (n_b - 1) tokens
+ *   sel_idx         int32 [B][num_kv_heads][budget_pages]
+ *   sel_cnt         int32 [B][num_kv_heads]
+ */
+#ifndef SVQUEST_H
+#define SVQUEST_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum sv_status {
+    SV_OK = 0,
+    SV_ERR_INVALID_ARG = 1,   /* NULL pointer, negative or inconsistent size */
+    SV_ERR_UNSUPPORTED = 2,   /* geometry this build does not support */
+    SV_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than required */
+    SV_ERR_CUDA = 4           /* a kernel launch or device query failed */
+};
+
+/* Device error-word bits (sv_get_device_error). */
+#define SV_DEVERR_PAGE_TABLE 0x1u   /* page_table entry outside [0, num_phys_pages) */
+#define SV_DEVERR_SEL_IDX    0x2u   /* sel_idx entry outside [0, n_b) or sel_cnt out of range */
+#define SV_DEVERR_SLOT       0x4u   /* slot_mapping entry outside the pool */
+#define SV_DEVERR_SEQ_LEN    0x8u   /* seq_lens[b] < 1 or needs more than max_pages pages */
+
+/* The paged pool and its metadata: caller-owned device buffers. */
+typedef struct sv_cache {
+    void* k_pool;             /* bf16 [num_phys_pages][num_kv_heads][16][128] */
+    void* v_pool;             /* bf16 [num_phys_pages][num_kv_heads][16][128] */
+    void* meta;               /* bf16 [num_phys_pages][num_kv_heads][2][128]  */
+    int64_t num_phys_pages;
+    int32_t num_kv_heads;
+    int32_t page_size;        /* must be 16 */
+    int32_t head_dim;         /* must be 128 */
+} sv_cache;
+
+/*
+ * sv_quest_update_meta -- the on_kv_stored hook ("add-sparse-method" page,
+ * "Placement Rules" item 3: metadata is updated after KV is written).
+ * Writes T new tokens' key and value rows into the pool at
+ * slot = physical_page * 16 + offset, and refreshes the touched pages'
+ * per-channel key min/max: a page whose run of new tokens starts at offset 0
+ * restarts its metadata from those tokens; otherwise the new tokens are
+ * folded into the stored min/max.  min/max of bf16 values are bf16 values,
+ * so the metadata is exact.
+ *   k_new, v_new   bf16 [T][num_kv_heads][128]
+ *   slot_mapping   int32 [T]
+ * Contract: within one call, the tokens of one page are consecutive in the
+ * token list with increasing offsets; across calls, each page fills from
+ * offset 0 without holes.  T == 0 is a no-op.
+ */
+int sv_quest_update_meta(const sv_cache* cache, const void* k_new, const void* v_new,
+                         const int32_t* slot_mapping, int64_t num_tokens, void* stream);
+
+/*
+ * sv_quest_score -- the page-scoring half of build_decode_view.  For every
+ * request b, kv head g and logical page p < n_b:
+ *   scores[b][g][p] = sum over the query heads h of group g, over channels i,
+ *                     of max(q[h][i] * kmax[i], q[h][i] * kmin[i])
+ * computed in fp32 as sum_i Qp[i] * kmax[i] + Qn[i] * kmin[i] with
+ * Qp = sum_h max(q_h, 0) and Qn = sum_h min(q_h, 0), which is the same sum
+ * regrouped by the sign of each q.  Entries p >= n_b are not written.
+ *   scores   fp32 [B][num_kv_heads][max_pages]
+ */
+int sv_quest_score(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                   const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                   int32_t max_pages, float* scores, void* stream);
+
+/*
+ * sv_quest_topk -- the selection half of build_decode_view ("Quest's
+ * query-relevant page selection", SparseEngine page, "method key points").
+ * For each (b, g) keeps the K_b = min(budget_pages, n_b) pages with the
+ * highest score; among equal scores the lower logical page index wins.
+ * Writes their logical indices in ascending order to sel_idx[b][g][0..K_b),
+ * -1 to the rest of the row, and K_b to sel_cnt[b][g].
+ * max_pages <= 32768.
+ */
+int sv_quest_topk(const float* scores, const int32_t* seq_lens, int32_t batch,
+                  int32_t num_kv_heads, int32_t max_pages, int32_t budget_pages,
+                  int32_t* sel_idx, int32_t* sel_cnt, void* stream);
+
+/*
+ * sv_quest_select -- build_decode_view in one call: sv_quest_score then
+ * sv_quest_topk.  Scores go to scores_out when it is non-NULL (fp32
+ * [B][num_kv_heads][max_pages]), else to the workspace, which must then hold
+ * sv_quest_select_workspace_size(...) bytes (ws may be NULL when scores_out
+ * is given).
+ */
+int sv_quest_select(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                    const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                    int32_t max_pages, int32_t budget_pages, int32_t* sel_idx, int32_t* sel_cnt,
+                    float* scores_out, void* workspace, size_t workspace_bytes, void* stream);
+
+size_t sv_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t max_pages);
+
+/*
+ * sv_sparse_decode -- exact softmax attention of each query head over the
+ * tokens of its kv head's selected pages (the AttentionView consumed by a
+ * generic attention backend; SparseEngine page, "method key points").
+ * With sel_idx == NULL every page 0..n_b-1 is read (dense decode).
+ *   z_t = (q_h . k_t) * softmax_scale over the valid tokens t of the pages,
+ *   out[b][h] = sum_t softmax(z)_t v_t        bf16 [B][num_q_heads][128]
+ *   lse[b][h] = ln(sum_t exp(z_t))            fp32 [B][num_q_heads]
+ * A head with no token gets out = 0, lse = -inf.  Split-K: each (request,
+ * kv head) is cut into page ranges whose partial (max, sum, output) go to
+ * the workspace and are merged by a log-sum-exp combine.
+ * budget_pages is the row length of sel_idx (ignored when dense).
+ */
+int sv_sparse_decode(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                     const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                     int32_t max_pages, const int32_t* sel_idx, const int32_t* sel_cnt,
+                     int32_t budget_pages, float softmax_scale, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* pages = budget_pages for sparse decode, max_pages for dense decode. */
+size_t sv_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t pages);
+
+/* Reads (and with reset != 0 clears) the current device's error word; the
+ * read synchronises the device.  Returns SV_OK or SV_ERR_CUDA. */
+int sv_get_device_error(uint32_t* flags, int reset);
+
+const char* sv_status_string(int status);
+int sv_version(void);   /* major * 10000 + minor * 100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVQUEST_H */

@@ -1,0 +1,186 @@
+"""Thin ctypes binding of libsvquest.so (include/svquest.h).
+
+Argument marshalling only: every function takes torch tensors that already
+live on the GPU, passes their data pointers, sizes and the current CUDA
+stream to the C ABI function of the same name, and raises SvError on a
+nonzero status.  There is no CPU fallback: if the library is missing the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from .build import LIB_PATH
+
+_lib = None
+
+
+class SvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _load().sv_status_string(status).decode()
+        super().__init__(f"{fn} failed: {msg}")
+        self.status = status
+
+
+class sv_cache(ctypes.Structure):
+    _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("meta", ctypes.c_void_p),
+                ("num_phys_pages", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libsvquest.so not built ({LIB_PATH}); run "
+                           "`python -m query_aware_sparse_quest_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    cp = ctypes.POINTER(sv_cache)
+    sig = {
+        "sv_quest_update_meta": [cp, vp, vp, vp, i64, vp],
+        "sv_quest_score": [cp, vp, i32, vp, vp, i32, i32, vp, vp],
+        "sv_quest_topk": [vp, vp, i32, i32, i32, i32, vp, vp, vp],
+        "sv_quest_select": [cp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp],
+        "sv_sparse_decode": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp, sz, vp],
+        "sv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int],
+    }
+    for name, args in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = ctypes.c_int
+    lib.sv_quest_select_workspace_size.argtypes = [i32, i32, i32]
+    lib.sv_quest_select_workspace_size.restype = sz
+    lib.sv_sparse_decode_workspace_size.argtypes = [i32, i32, i32, i32]
+    lib.sv_sparse_decode_workspace_size.restype = sz
+    lib.sv_status_string.argtypes = [ctypes.c_int]
+    lib.sv_status_string.restype = ctypes.c_char_p
+    lib.sv_version.argtypes = []
+    lib.sv_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _p(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise SvError(fn, status)
+
+
+class Cache:
+    """A paged pool on the device: k/v bf16 [pages][Hkv][16][128], meta bf16 [pages][Hkv][2][128]."""
+
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, meta: torch.Tensor):
+        self.k_pool, self.v_pool, self.meta = k_pool, v_pool, meta
+        n, hkv, p, d = k_pool.shape
+        self.c = sv_cache(k_pool.data_ptr(), v_pool.data_ptr(), meta.data_ptr(), n, hkv, p, d)
+
+    @classmethod
+    def empty(cls, num_phys_pages: int, num_kv_heads: int, device="cuda", page_size: int = 16,
+              head_dim: int = 128) -> "Cache":
+        shape = (num_phys_pages, num_kv_heads, page_size, head_dim)
+        k = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        v = torch.zeros(shape, dtype=torch.bfloat16, device=device)
+        m = torch.zeros((num_phys_pages, num_kv_heads, 2, head_dim), dtype=torch.bfloat16, device=device)
+        return cls(k, v, m)
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.c.num_kv_heads)
+
+    def ref(self):
+        return ctypes.byref(self.c)
+
+
+def sv_quest_update_meta(cache: Cache, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                         stream=None) -> None:
+    _check("sv_quest_update_meta", _load().sv_quest_update_meta(
+        cache.ref(), _p(k_new), _p(v_new), _p(slot_mapping), int(slot_mapping.numel()), _stream(stream)))
+
+
+def sv_quest_score(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                   scores: torch.Tensor, stream=None) -> None:
+    B, Hq, _ = q.shape
+    _check("sv_quest_score", _load().sv_quest_score(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(scores),
+        _stream(stream)))
+
+
+def sv_quest_topk(scores: torch.Tensor, seq_lens: torch.Tensor, budget_pages: int, sel_idx: torch.Tensor,
+                  sel_cnt: torch.Tensor, stream=None) -> None:
+    B, Hkv, max_pages = scores.shape
+    _check("sv_quest_topk", _load().sv_quest_topk(
+        _p(scores), _p(seq_lens), B, Hkv, max_pages, int(budget_pages), _p(sel_idx), _p(sel_cnt), _stream(stream)))
+
+
+def sv_quest_select_workspace_size(batch: int, num_kv_heads: int, max_pages: int) -> int:
+    return int(_load().sv_quest_select_workspace_size(batch, num_kv_heads, max_pages))
+
+
+def sv_quest_select(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                    budget_pages: int, sel_idx: torch.Tensor, sel_cnt: torch.Tensor,
+                    scores_out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                    stream=None) -> None:
+    B, Hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sv_quest_select", _load().sv_quest_select(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
+        _p(sel_idx), _p(sel_cnt), _p(scores_out), _p(workspace), ws_bytes, _stream(stream)))
+
+
+def sv_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, pages: int) -> int:
+    return int(_load().sv_sparse_decode_workspace_size(batch, num_q_heads, num_kv_heads, pages))
+
+
+def sv_sparse_decode(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                     sel_idx: Optional[torch.Tensor], sel_cnt: Optional[torch.Tensor], out: torch.Tensor,
+                     lse: torch.Tensor, workspace: torch.Tensor, softmax_scale: Optional[float] = None,
+                     stream=None) -> None:
+    B, Hq, D = q.shape
+    K = 0 if sel_idx is None else int(sel_idx.shape[2])
+    scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
+    _check("sv_sparse_decode", _load().sv_sparse_decode(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
+        _p(sel_cnt), K, scale, _p(out), _p(lse), _p(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)))
+
+
+def sv_get_device_error(reset: bool = True) -> int:
+    flags = ctypes.c_uint32(0)
+    _check("sv_get_device_error", _load().sv_get_device_error(ctypes.byref(flags), int(reset)))
+    return int(flags.value)
+
+
+def sv_status_string(status: int) -> str:
+    return _load().sv_status_string(status).decode()
+
+
+def sv_version() -> int:
+    return int(_load().sv_version())
+
+
+def raw_library():
+    """The loaded ctypes library, for calls made with raw pointers."""
+    return _load()

@@ -1,0 +1,192 @@
+// C ABI of libsvquest.so (include/svquest.h): host-side argument checks,
+// launch-shape choices and dispatch to the kernels.  Nothing here allocates,
+// frees or synchronises, except sv_get_device_error which reads device words.
+#include <climits>
+
+#include "svq_common.cuh"
+
+namespace svq {
+int read_error_meta(uint32_t* flags, int reset);
+int read_error_select(uint32_t* flags, int reset);
+int read_error_decode(uint32_t* flags, int reset);
+int launch_update_meta(const sv_cache* c, const void* k_new, const void* v_new, const int32_t* slot_mapping,
+                       int64_t num_tokens, cudaStream_t stream);
+int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
+                 const int32_t* seq_lens, int batch, int max_pages, float* scores, int sm_count,
+                 cudaStream_t stream);
+int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
+                int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, cudaStream_t stream);
+int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
+                  const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
+                  const int32_t* sel_cnt, int budget_pages, float softmax_scale, void* out, float* lse,
+                  void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream);
+int decode_max_splits(int pages);
+size_t decode_workspace_bytes(int batch, int num_q_heads, int splits);
+
+constexpr int kMaxTopkPages = 32768;
+
+namespace {
+
+int sm_count_of_current_device(int* out) {
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
+        *out = cached[dev];
+        return SV_OK;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+        return SV_ERR_CUDA;
+    if (dev >= 0 && dev < 64) cached[dev] = n;
+    *out = n;
+    return SV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_cache(const sv_cache* c) {
+    if (!c || !c->k_pool || !c->v_pool || !c->meta) return SV_ERR_INVALID_ARG;
+    if (c->num_phys_pages < 1 || c->num_kv_heads < 1) return SV_ERR_INVALID_ARG;
+    if (c->num_phys_pages > INT_MAX) return SV_ERR_UNSUPPORTED;
+    if (c->page_size != kPage || c->head_dim != kHeadDim) return SV_ERR_UNSUPPORTED;
+    if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->meta)) return SV_ERR_INVALID_ARG;
+    return SV_OK;
+}
+
+int check_heads(const sv_cache* c, int num_q_heads) {
+    if (num_q_heads < 1 || num_q_heads % c->num_kv_heads != 0) return SV_ERR_INVALID_ARG;
+    if (num_q_heads / c->num_kv_heads > kMaxGroup) return SV_ERR_UNSUPPORTED;
+    return SV_OK;
+}
+
+int check_batch(const void* q, const int32_t* page_table, const int32_t* seq_lens, int batch, int max_pages) {
+    if (!q || !page_table || !seq_lens) return SV_ERR_INVALID_ARG;
+    if (batch < 1 || max_pages < 1) return SV_ERR_INVALID_ARG;
+    if (batch > 65535) return SV_ERR_UNSUPPORTED;
+    if (!aligned16(q)) return SV_ERR_INVALID_ARG;
+    return SV_OK;
+}
+
+size_t scores_bytes(int batch, int num_kv_heads, int max_pages) {
+    return (static_cast<size_t>(batch) * num_kv_heads * max_pages * sizeof(float) + 255) / 256 * 256;
+}
+
+}  // namespace
+}  // namespace svq
+
+using namespace svq;
+
+extern "C" {
+
+int sv_quest_update_meta(const sv_cache* cache, const void* k_new, const void* v_new,
+                         const int32_t* slot_mapping, int64_t num_tokens, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if (num_tokens < 0) return SV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return SV_OK;
+    if (!k_new || !v_new || !slot_mapping) return SV_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new)) return SV_ERR_INVALID_ARG;
+    return launch_update_meta(cache, k_new, v_new, slot_mapping, num_tokens, static_cast<cudaStream_t>(stream));
+}
+
+int sv_quest_score(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                   const int32_t* seq_lens, int32_t batch, int32_t max_pages, float* scores, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if (!scores) return SV_ERR_INVALID_ARG;
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    return launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms,
+                        static_cast<cudaStream_t>(stream));
+}
+
+int sv_quest_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int32_t num_kv_heads,
+                  int32_t max_pages, int32_t budget_pages, int32_t* sel_idx, int32_t* sel_cnt, void* stream) {
+    if (!scores || !seq_lens || !sel_idx || !sel_cnt) return SV_ERR_INVALID_ARG;
+    if (batch < 1 || num_kv_heads < 1 || max_pages < 1 || budget_pages < 1) return SV_ERR_INVALID_ARG;
+    if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * num_kv_heads > INT_MAX) return SV_ERR_UNSUPPORTED;
+    return launch_topk(scores, seq_lens, batch, num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt,
+                       static_cast<cudaStream_t>(stream));
+}
+
+size_t sv_quest_select_workspace_size(int32_t batch, int32_t num_kv_heads, int32_t max_pages) {
+    if (batch < 1 || num_kv_heads < 1 || max_pages < 1) return 0;
+    return scores_bytes(batch, num_kv_heads, max_pages);
+}
+
+int sv_quest_select(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                    const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                    int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if (!sel_idx || !sel_cnt || budget_pages < 1) return SV_ERR_INVALID_ARG;
+    if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
+    float* scores = scores_out;
+    if (!scores) {
+        if (!workspace || workspace_bytes < scores_bytes(batch, cache->num_kv_heads, max_pages))
+            return SV_ERR_WORKSPACE;
+        scores = static_cast<float*>(workspace);
+    }
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms, s)))
+        return st;
+    return launch_topk(scores, seq_lens, batch, cache->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, s);
+}
+
+size_t sv_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t pages) {
+    if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || pages < 1) return 0;
+    return decode_workspace_bytes(batch, num_q_heads, decode_max_splits(pages));
+}
+
+int sv_sparse_decode(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                     const int32_t* seq_lens, int32_t batch, int32_t max_pages, const int32_t* sel_idx,
+                     const int32_t* sel_cnt, int32_t budget_pages, float softmax_scale, void* out, float* lse,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if (!out || !lse) return SV_ERR_INVALID_ARG;
+    if (sel_idx && (!sel_cnt || budget_pages < 1)) return SV_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(batch) * cache->num_kv_heads > 65535) return SV_ERR_UNSUPPORTED;
+    if (!workspace) return SV_ERR_WORKSPACE;
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
+                         budget_pages, softmax_scale, out, lse, workspace, workspace_bytes, sms,
+                         static_cast<cudaStream_t>(stream));
+}
+
+int sv_get_device_error(uint32_t* flags, int reset) {
+    if (!flags) return SV_ERR_INVALID_ARG;
+    *flags = 0;
+    int st;
+    if ((st = read_error_meta(flags, reset))) return st;
+    if ((st = read_error_select(flags, reset))) return st;
+    return read_error_decode(flags, reset);
+}
+
+const char* sv_status_string(int status) {
+    switch (status) {
+        case SV_OK: return "SV_OK";
+        case SV_ERR_INVALID_ARG: return "SV_ERR_INVALID_ARG: null pointer, misaligned buffer or bad size";
+        case SV_ERR_UNSUPPORTED: return "SV_ERR_UNSUPPORTED: geometry not supported by this build";
+        case SV_ERR_WORKSPACE: return "SV_ERR_WORKSPACE: workspace missing or too small";
+        case SV_ERR_CUDA: return "SV_ERR_CUDA: CUDA launch or device query failed";
+        default: return "unknown sv_status";
+    }
+}
+
+int sv_version(void) { return 100; }
+
+}  // extern "C"

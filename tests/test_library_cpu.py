@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side
+argument checks reject bad calls before any launch (no GPU needed)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch  # noqa: F401  (loads the CUDA runtime the library links against)
+
+from query_aware_sparse_quest_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "svquest.h")
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.raw_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("sv_quest_update_meta", "sv_quest_select", "sv_sparse_decode"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert binding.sv_status_string(0) == "SV_OK"
+    for st in (1, 2, 3, 4):
+        assert binding.sv_status_string(st).startswith("SV_ERR")
+    assert binding.sv_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    # scores: B * Hkv * max_pages fp32, rounded up to 256 bytes
+    assert binding.sv_quest_select_workspace_size(8, 4, 8000) == 8 * 4 * 8000 * 4
+    assert binding.sv_quest_select_workspace_size(1, 1, 3) == 256
+    assert binding.sv_quest_select_workspace_size(0, 4, 10) == 0
+    # decode partials: at most 64 splits, at least 8 pages per split
+    ws = binding.sv_sparse_decode_workspace_size(8, 32, 4, 256)
+    assert ws >= 8 * 32 * 32 * (128 * 4 + 8)
+    assert binding.sv_sparse_decode_workspace_size(8, 32, 4, 8000) >= 8 * 32 * 64 * 128 * 4
+    assert binding.sv_sparse_decode_workspace_size(1, 4, 1, 1) >= 4 * (128 * 4 + 8)
+
+
+def _fake_cache(page_size=16, head_dim=128, hkv=4, pages=10, null=False):
+    # Host-side checks only read the struct; these addresses are never dereferenced.
+    addr = 0 if null else 0x10000
+    return binding.sv_cache(addr, addr, addr, pages, hkv, page_size, head_dim)
+
+
+FAKE = ctypes.c_void_p(0x20000)
+
+
+@pytest.mark.parametrize("cache,hq,expect", [
+    (_fake_cache(null=True), 32, SV_ERR_INVALID_ARG),
+    (_fake_cache(page_size=32), 32, SV_ERR_UNSUPPORTED),
+    (_fake_cache(head_dim=64), 32, SV_ERR_UNSUPPORTED),
+    (_fake_cache(hkv=4), 30, SV_ERR_INVALID_ARG),       # Hq not a multiple of Hkv
+    (_fake_cache(hkv=1), 16, SV_ERR_UNSUPPORTED),       # 16 query heads per kv head
+    (_fake_cache(pages=0), 32, SV_ERR_INVALID_ARG),
+])
+def test_select_rejects_bad_geometry(lib, cache, hq, expect):
+    st = lib.sv_quest_select(ctypes.byref(cache), FAKE, hq, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None,
+                             FAKE, 1 << 20, None)
+    assert st == expect
+
+
+def test_select_rejects_bad_sizes(lib):
+    c = ctypes.byref(_fake_cache())
+    assert lib.sv_quest_select(c, None, 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, FAKE, 1 << 20, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 0, 100, 16, FAKE, FAKE, None, FAKE, 1 << 20, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 8, 100, 0, FAKE, FAKE, None, FAKE, 1 << 20, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 8, 40000, 16, FAKE, FAKE, None, FAKE, 1 << 30, None) == SV_ERR_UNSUPPORTED
+    # scores need 8*4*100*4 bytes of workspace when scores_out is NULL
+    assert lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, FAKE, 100, None) == SV_ERR_WORKSPACE
+    assert lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, None, 1 << 20, None) == SV_ERR_WORKSPACE
+    # misaligned q
+    assert lib.sv_quest_select(c, ctypes.c_void_p(0x20002), 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, FAKE,
+                               1 << 20, None) == SV_ERR_INVALID_ARG
+
+
+def test_topk_rejects_bad_args(lib):
+    assert lib.sv_quest_topk(None, FAKE, 8, 4, 100, 16, FAKE, FAKE, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_topk(FAKE, FAKE, 8, 4, 100, 0, FAKE, FAKE, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_topk(FAKE, FAKE, 8, 4, 32769, 16, FAKE, FAKE, None) == SV_ERR_UNSUPPORTED
+
+
+def test_decode_rejects_bad_args(lib):
+    c = ctypes.byref(_fake_cache())
+    ok = dict(q=FAKE, pt=FAKE, sl=FAKE, out=FAKE, lse=FAKE, ws=FAKE)
+
+    def call(scale=0.088, sel=None, cnt=None, K=0, ws=FAKE, out=FAKE, hq=32, batch=8):
+        return lib.sv_sparse_decode(c, ok["q"], hq, ok["pt"], ok["sl"], batch, 100, sel, cnt, K, scale, out,
+                                    ok["lse"], ws, 1 << 20, None)
+    assert call(out=None) == SV_ERR_INVALID_ARG
+    assert call(scale=0.0) == SV_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == SV_ERR_INVALID_ARG
+    assert call(sel=FAKE, cnt=None, K=16) == SV_ERR_INVALID_ARG
+    assert call(sel=FAKE, cnt=FAKE, K=0) == SV_ERR_INVALID_ARG
+    assert call(ws=None) == SV_ERR_WORKSPACE
+    assert call(hq=33) == SV_ERR_INVALID_ARG
+
+
+def test_update_meta_rejects_bad_args(lib):
+    c = ctypes.byref(_fake_cache())
+    assert lib.sv_quest_update_meta(c, FAKE, FAKE, FAKE, -1, None) == SV_ERR_INVALID_ARG
+    assert lib.sv_quest_update_meta(c, FAKE, FAKE, FAKE, 0, None) == SV_OK       # no-op, nothing launched
+    assert lib.sv_quest_update_meta(c, None, FAKE, FAKE, 4, None) == SV_ERR_INVALID_ARG
+    bad = ctypes.byref(_fake_cache(page_size=8))
+    assert lib.sv_quest_update_meta(bad, FAKE, FAKE, FAKE, 4, None) == SV_ERR_UNSUPPORTED
