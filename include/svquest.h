@@ -155,6 +155,33 @@ int sv_sparse_decode(const sv_cache* cache, const void* q, int32_t num_q_heads,
 size_t sv_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                        int32_t pages);
 
+/*
+ * sv_sparse_decode_static_scratch -- sv_sparse_decode without a caller
+ * workspace; the paper has no counterpart to this call.  It is for callers
+ * that cannot allocate device memory: plugins inside a host framework that
+ * owns every device allocation and forbids cudaMalloc, or serving loops that
+ * reserved nearly all of HBM for the KV cache up front.  The split-K
+ * partials go to a 16 MiB array compiled into the library (every GPU that
+ * loads the library holds it until the process exits).  The call allocates
+ * nothing; inputs and outputs are still the caller's.
+ *  - The first call on a device looks up that device's address of the array
+ *    (a runtime symbol query); make that first call before any stream capture.
+ *  - Every call shares the one array: calls whose kernels may overlap on the
+ *    GPU (other streams, other threads) race on it and must be serialised by
+ *    the caller.  Nothing in it needs to start at zero.
+ *  - Returns SV_ERR_WORKSPACE, launching nothing, when
+ *    sv_sparse_decode_workspace_size(batch, num_q_heads, num_kv_heads, pages)
+ *    exceeds SV_STATIC_SCRATCH_BYTES (e.g. batch 8 x 32 query heads fits at
+ *    any budget; batch 32 x 32 heads fits up to 248 pages, not beyond).
+ * Arguments and results are those of sv_sparse_decode.
+ */
+#define SV_STATIC_SCRATCH_BYTES (16u << 20)
+int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                                    const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                    int32_t max_pages, const int32_t* sel_idx, const int32_t* sel_cnt,
+                                    int32_t budget_pages, float softmax_scale, void* out, float* lse,
+                                    void* stream);
+
 /* Reads (and with reset != 0 clears) the current device's error word; the
  * read synchronises the device.  Returns SV_OK or SV_ERR_CUDA. */
 int sv_get_device_error(uint32_t* flags, int reset);

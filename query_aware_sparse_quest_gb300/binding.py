@@ -52,6 +52,7 @@ def _load():
         "sv_quest_topk": [vp, vp, i32, i32, i32, i32, vp, vp, vp],
         "sv_quest_select": [cp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp],
         "sv_sparse_decode": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp, sz, vp],
+        "sv_sparse_decode_static_scratch": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp],
         "sv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int],
     }
     for name, args in sig.items():
@@ -165,6 +166,19 @@ def sv_sparse_decode(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, se
         cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
         _p(sel_cnt), K, scale, _p(out), _p(lse), _p(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream)))
+
+
+def sv_sparse_decode_static_scratch(cache: Cache, q: torch.Tensor, page_table: torch.Tensor,
+                                    seq_lens: torch.Tensor, sel_idx: Optional[torch.Tensor],
+                                    sel_cnt: Optional[torch.Tensor], out: torch.Tensor, lse: torch.Tensor,
+                                    softmax_scale: Optional[float] = None, stream=None) -> None:
+    """sv_sparse_decode with the library's fixed scratch array instead of a workspace."""
+    B, Hq, D = q.shape
+    K = 0 if sel_idx is None else int(sel_idx.shape[2])
+    scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
+    _check("sv_sparse_decode_static_scratch", _load().sv_sparse_decode_static_scratch(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
+        _p(sel_cnt), K, scale, _p(out), _p(lse), _stream(stream)))
 
 
 def sv_get_device_error(reset: bool = True) -> int:
