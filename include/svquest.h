@@ -61,6 +61,7 @@ enum sv_status {
 #define SV_DEVERR_SEL_IDX    0x2u   /* sel_idx entry outside [0, n_b) or sel_cnt out of range */
 #define SV_DEVERR_SLOT       0x4u   /* slot_mapping entry outside the pool */
 #define SV_DEVERR_SEQ_LEN    0x8u   /* seq_lens[b] < 1 or needs more than max_pages pages */
+#define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up waiting for its own bulk copies */
 
 /* The paged pool and its metadata: caller-owned device buffers. */
 typedef struct sv_cache {

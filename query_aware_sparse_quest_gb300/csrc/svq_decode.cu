@@ -17,12 +17,18 @@ namespace svq {
 
 SVQ_DEFINE_ERROR_WORD(read_error_decode)
 
-constexpr int kDecodeWarps = 4;
-constexpr int kDecodeThreads = kDecodeWarps * 32;
-constexpr int kStages = 3;                        // pages in flight per warp
-constexpr int kTileBytes = kPage * kHeadDim * 2;  // 4 KB: one page of K (or V) for one kv head
+#ifndef SVQ_DEC_STAGES
+#define SVQ_DEC_STAGES 6
+#endif
+constexpr int kConsumers = 4;                     // consumer warps; warp w owns channels 32w .. 32w+31
+constexpr int kDecodeThreads = (kConsumers + 1) * 32;
+constexpr int kProducer = kConsumers;             // warp index of the producer
+constexpr int kStages = SVQ_DEC_STAGES;           // pages in flight per CTA
+constexpr int kRowBytes = kHeadDim * 2;           // one token's key (or value) row: 256 B
+constexpr int kRowStride = kRowBytes + 16;        // padded shared-memory row (conflict-free ldmatrix)
+constexpr int kTileBytes = kPage * kRowStride;    // one page of K (or V) for one kv head
 constexpr int kStageBytes = 2 * kTileBytes;       // K + V
-constexpr int kDecodeSmem = kDecodeWarps * kStages * kStageBytes;
+constexpr int kDecodeSmem = kStages * kStageBytes;
 constexpr int kMaxSplits = 64;
 constexpr int kMinPagesPerSplit = 8;
 
@@ -46,9 +52,28 @@ struct DecodeArgs {
     float2* ml_part;          // [B][Hq][S] (running max in log2 units, sum of exp2)
 };
 
-__global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const DecodeArgs a) {
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// One CTA per (split, request, kv head).  A producer warp resolves the
+// split's pages (selection list -> logical page -> physical page) and moves
+// each page's key and value rows into a kStages-deep ring with 256-byte bulk
+// copies (lane r: key row r, lane 16 + r: value row r), completing on the
+// stage's "full" mbarrier; rows past the page's fill are not copied, and the
+// value rows among them are zeroed.  Each of the four consumer warps computes
+// the page's logits S^T = K Q^T for the whole query group (the same values
+// in every warp), runs the same online softmax, and accumulates its own 32
+// output channels O^T += V^T P^T; it then arrives on the stage's "empty"
+// mbarrier so the producer can refill it.  Because every consumer holds the
+// same running max and sum, the CTA's partial needs no cross-warp merge.
+__global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int s_valid[kDecodeWarps][kStages];
+    __shared__ int s_valid[kStages];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
 
     const int split = blockIdx.x;
     const int bg = blockIdx.y;
@@ -56,8 +81,18 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     const int g = bg % a.num_kv_heads;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int quad = lane & 3;      // column pair of the accumulator fragments
-    const int row = lane >> 2;      // row of the accumulator fragments
+    const uint32_t ring_s = smem_addr(smem);
+    const uint32_t full0 = smem_addr(&full_bar[0]);
+    const uint32_t empty0 = smem_addr(&empty_bar[0]);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kStages; ++st) {
+            mbar_init(full0 + st * 8, 1);
+            mbar_init(empty0 + st * 8, kConsumers);
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
 
     const int len = a.seq_lens[b];
     int n = (len + kPage - 1) / kPage;
@@ -65,23 +100,96 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         if (threadIdx.x == 0 && split == 0) svq_flag(SV_DEVERR_SEQ_LEN);
         n = len < 1 ? 0 : a.max_pages;
     }
-    int count = n;
-    if (a.sel_idx) {
-        count = a.sel_cnt[bg];
-        if (count < 0 || count > a.K || count > n) {
-            if (threadIdx.x == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
-            count = max(0, min(count, min(a.K, n)));
+
+    if (warp == kProducer) {
+        const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
+        const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
+        pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
+        int count = n;
+        if (a.sel_idx) {
+            count = a.sel_cnt[bg];
+            if (count < 0 || count > a.K || count > n) {
+                if (lane == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
+                count = max(0, min(count, min(a.K, n)));
+            }
         }
+        const int chunk = (count + a.num_splits - 1) / a.num_splits;
+        const int j0 = min(count, split * chunk);
+        const int my_count = min(count, j0 + chunk) - j0;
+        // Resolve 32 pages at a time: lane l handles list position base + l.
+        int pl_phys = 0, pl_valid = 0, pl_base = -32;
+        bool failed = false;
+        int issued = 0;
+        for (int i = 0; i < my_count && !failed; ++i) {
+            if (i >= pl_base + 32) {
+                pl_base += 32;
+                const int ii = pl_base + lane;
+                pl_phys = 0;
+                pl_valid = 0;
+                if (ii < my_count) {
+                    const int j = j0 + ii;
+                    const int lp = sel_row ? sel_row[j] : j;
+                    if (lp < 0 || lp >= n) {
+                        svq_flag(SV_DEVERR_SEL_IDX);
+                    } else {
+                        const int ph = pt_row[lp];
+                        if (ph < 0 || ph >= a.num_phys_pages) {
+                            svq_flag(SV_DEVERR_PAGE_TABLE);
+                        } else {
+                            pl_phys = ph;
+                            pl_valid = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
+                        }
+                    }
+                }
+            }
+            const int stage = i % kStages;
+            if (i >= kStages) {
+                const bool ok = mbar_wait_bounded(empty0 + stage * 8, ((i / kStages) - 1) & 1);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    failed = true;
+                    break;
+                }
+            }
+            const int64_t phys = __shfl_sync(0xffffffffu, pl_phys, i - pl_base);
+            const int valid = __shfl_sync(0xffffffffu, pl_valid, i - pl_base);
+            unsigned char* st_ptr = smem + stage * kStageBytes;
+            if (valid < kPage) {
+                for (int c = lane; c < (kPage - valid) * 16; c += 32) {
+                    const int rr = valid + (c >> 4);
+                    *reinterpret_cast<uint4*>(st_ptr + kTileBytes + rr * kRowStride + (c & 15) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            const uint32_t fb = full0 + stage * 8;
+            if (lane == 0) {
+                s_valid[stage] = valid;
+                if (valid > 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(valid) * 2 * kRowBytes);
+                else mbar_arrive(fb);
+            }
+            __syncwarp();
+            const int r = lane & 15;
+            if (r < valid) {
+                const int64_t row = (phys * a.num_kv_heads + g) * (kPage * kHeadDim) + r * kHeadDim;
+                bulk_copy_g2s(ring_s + stage * kStageBytes + (lane < 16 ? 0 : kTileBytes) + r * kRowStride,
+                              (lane < 16 ? a.k_pool : a.v_pool) + row, kRowBytes, fb);
+            }
+            ++issued;
+        }
+        if (failed) {
+            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
+        }
+        // Every copy of this CTA lands before the CTA (and its shared memory) retires.
+        for (int p = max(0, issued - kStages); p < issued; ++p)
+            (void)mbar_wait_bounded(full0 + (p % kStages) * 8, (p / kStages) & 1);
+        pdl_launch_dependents();
+        return;
     }
-    const int chunk = (count + a.num_splits - 1) / a.num_splits;
-    const int j0 = min(count, split * chunk);
-    const int j1 = min(count, j0 + chunk);
-    // Pages of this warp: list positions j0 + warp + kDecodeWarps * i.
-    const int my_count = (j1 - j0 > warp) ? (j1 - j0 - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
 
-    unsigned char* wbuf = smem + warp * kStages * kStageBytes;
-    const uint32_t wbuf_s = smem_addr(wbuf);
-
+    // ---------------- consumer warps
+    const int quad = lane & 3;      // column pair of the accumulator fragments
+    const int row = lane >> 2;      // row of the accumulator fragments
     // Q^T fragments (B operand): head `row` of the group, channels 16kk + 2 quad (+8).
     uint32_t qf[8][2];
     {
@@ -93,79 +201,50 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
             qf[kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * quad) : 0u;
         }
     }
+    pdl_wait();
+    // The producer's page count for this CTA (same formula, computed again here).
+    int count = n;
+    if (a.sel_idx) count = max(0, min(a.sel_cnt[bg], min(a.K, n)));
+    const int chunk = (count + a.num_splits - 1) / a.num_splits;
+    const int j0 = min(count, split * chunk);
+    const int my_count = min(count, j0 + chunk) - j0;
 
-    const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
-    const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
-
-    auto issue = [&](int i, int stage) {
-        const int j = j0 + warp + kDecodeWarps * i;
-        int lp = sel_row ? sel_row[j] : j;
-        int valid = 0;
-        int64_t phys = 0;
-        if (lp < 0 || lp >= n) {
-            if (lane == 0) svq_flag(SV_DEVERR_SEL_IDX);
-        } else {
-            phys = pt_row[lp];
-            if (phys < 0 || phys >= a.num_phys_pages) {
-                if (lane == 0) svq_flag(SV_DEVERR_PAGE_TABLE);
-                phys = 0;
-            } else {
-                valid = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
-            }
-        }
-        if (lane == 0) s_valid[warp][stage] = valid;
-        const int64_t tile = (phys * a.num_kv_heads + g) * (kPage * kHeadDim);
-        const unsigned char* ksrc = reinterpret_cast<const unsigned char*>(a.k_pool + tile);
-        const unsigned char* vsrc = reinterpret_cast<const unsigned char*>(a.v_pool + tile);
-        const uint32_t kdst = wbuf_s + stage * kStageBytes;
-        const uint32_t vdst = kdst + kTileBytes;
+    float o[2][4];
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-            const int c = lane + 32 * r;      // 16-byte chunk of the 4 KB tile
-            const int trow = c >> 4, tch = c & 15;
-            const uint32_t nbytes = trow < valid ? 16u : 0u;
-            cp_async16(kdst + tile_offset(trow, tch), ksrc + c * 16, nbytes);
-            cp_async16(vdst + tile_offset(trow, tch), vsrc + c * 16, nbytes);
-        }
-    };
-
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) {
-        if (st < my_count) issue(st, st);
-        cp_async_commit();
-    }
-
-    float o[8][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int t = 0; t < 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};   // heads 2 quad, 2 quad + 1 (log2 units)
     float l_run[2] = {0.f, 0.f};               // lane-partial sums
-
+    bool timed_out = false;
+    const int mat = lane >> 3, r8 = lane & 7;
     for (int i = 0; i < my_count; ++i) {
         const int stage = i % kStages;
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const uint32_t ks = wbuf_s + stage * kStageBytes;
+        const bool ok = mbar_wait_bounded(full0 + stage * 8, (i / kStages) & 1);
+        if (__any_sync(0xffffffffu, !ok)) {
+            timed_out = true;
+            break;
+        }
+        const uint32_t ks = ring_s + stage * kStageBytes;
         const uint32_t vs = ks + kTileBytes;
-        const int valid = s_valid[warp][stage];
+        const int valid = s_valid[stage];
 
-        // S^T (16 tokens x 8 heads) = K (16 x 128) Q^T (128 x 8)
-        float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T (16 tokens x 8 heads) = K (16 x 128) Q^T (128 x 8), two accumulation chains.
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            const int mat = lane >> 3, r = lane & 7;
-            const int trow = r + 8 * (mat & 1);
+            const uint32_t kaddr = ks + (r8 + 8 * (mat & 1)) * kRowStride + (mat >> 1) * 16;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
+            for (int kk = 0; kk < 8; kk += 2) {
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(ks + tile_offset(trow, 2 * kk + (mat >> 1)), a0, a1, a2, a3);
-                mma_bf16_16816(sacc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                ldmatrix_x4(kaddr + kk * 32, a0, a1, a2, a3);
+                mma_bf16_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                ldmatrix_x4(kaddr + (kk + 1) * 32, a0, a1, a2, a3);
+                mma_bf16_16816(sb, a0, a1, a2, a3, qf[kk + 1][0], qf[kk + 1][1]);
             }
         }
         // Scaled logits in log2 units; tokens past the page's fill are masked.
-        float x0 = row < valid ? sacc[0] * a.scale_log2 : -INFINITY;       // token row,   head 2q
-        float x1 = row < valid ? sacc[1] * a.scale_log2 : -INFINITY;       // token row,   head 2q+1
-        float x2 = row + 8 < valid ? sacc[2] * a.scale_log2 : -INFINITY;   // token row+8, head 2q
-        float x3 = row + 8 < valid ? sacc[3] * a.scale_log2 : -INFINITY;   // token row+8, head 2q+1
+        const float x0 = row < valid ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;       // token row,   head 2q
+        const float x1 = row < valid ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;       // token row,   head 2q+1
+        const float x2 = row + 8 < valid ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;   // token row+8, head 2q
+        const float x3 = row + 8 < valid ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;   // token row+8, head 2q+1
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int s = 4; s < 32; s <<= 1) {
@@ -175,19 +254,19 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
         const float base0 = mn0 == -INFINITY ? 0.f : mn0;
         const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float alpha0 = exp2f(m_run[0] - base0), alpha1 = exp2f(m_run[1] - base1);
-        const float p0 = exp2f(x0 - base0), p1 = exp2f(x1 - base1);
-        const float p2 = exp2f(x2 - base0), p3 = exp2f(x3 - base1);
+        const float alpha0 = fast_exp2(m_run[0] - base0), alpha1 = fast_exp2(m_run[1] - base1);
+        const float p0 = fast_exp2(x0 - base0), p1 = fast_exp2(x1 - base1);
+        const float p2 = fast_exp2(x2 - base0), p3 = fast_exp2(x3 - base1);
         m_run[0] = mn0;
         m_run[1] = mn1;
         l_run[0] = l_run[0] * alpha0 + p0 + p2;
         l_run[1] = l_run[1] * alpha1 + p1 + p3;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= alpha0;
-            o[mt][1] *= alpha1;
-            o[mt][2] *= alpha0;
-            o[mt][3] *= alpha1;
+        for (int t = 0; t < 2; ++t) {
+            o[t][0] *= alpha0;
+            o[t][1] *= alpha1;
+            o[t][2] *= alpha0;
+            o[t][3] *= alpha1;
         }
 
         // P^T as the B operand: lane needs P[token 2 quad + {0,1} (+8)][head row].
@@ -203,22 +282,21 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const uint32_t pb0 = __byte_perm(lo0, lo1, selector);
         const uint32_t pb1 = __byte_perm(hi0, hi1, selector);
 
-        // O^T (128 x 8) += V^T (128 x 16) P^T (16 x 8)
+        // O^T (this warp's 32 channels x 8) += V^T (32 x 16) P^T (16 x 8)
         {
-            const int mat = lane >> 3, r = lane & 7;
-            const int trow = r + 8 * (mat >> 1);
+            const uint32_t vaddr = vs + (r8 + 8 * (mat >> 1)) * kRowStride + (mat & 1) * 16;
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
+            for (int t = 0; t < 2; ++t) {
+                const int mt = 2 * warp + t;
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(vs + tile_offset(trow, 2 * mt + (mat & 1)), a0, a1, a2, a3);
-                mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+                ldmatrix_x4_trans(vaddr + mt * 32, a0, a1, a2, a3);
+                mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
             }
         }
-        __syncwarp();
-        if (i + kStages < my_count) issue(i + kStages, stage);
-        cp_async_commit();
+        __syncwarp();   // every lane has read the stage before it is released
+        if (lane == 0) mbar_arrive(empty0 + stage * 8);
     }
-    cp_async_wait<0>();
+    if (timed_out && lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
 
     // Full per-head sums over the 8 lanes sharing a head.
 #pragma unroll
@@ -226,76 +304,73 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], s);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], s);
     }
-
-    // Merge the warps of this CTA through shared memory (reusing the page buffers).
-    __syncthreads();
-    float* sm_o = reinterpret_cast<float*>(smem);                              // [warp][8][128]
-    float* sm_m = sm_o + kDecodeWarps * kMaxGroup * kHeadDim;                  // [warp][8]
-    float* sm_l = sm_m + kDecodeWarps * kMaxGroup;                             // [warp][8]
-    {
-        float* ow = sm_o + warp * kMaxGroup * kHeadDim;
-        const int h0 = 2 * quad, h1 = 2 * quad + 1;
+    const int S = a.num_splits;
+    const int h0 = 2 * quad, h1 = 2 * quad + 1;
+    const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            ow[h0 * kHeadDim + 16 * mt + row] = o[mt][0];
-            ow[h1 * kHeadDim + 16 * mt + row] = o[mt][1];
-            ow[h0 * kHeadDim + 16 * mt + row + 8] = o[mt][2];
-            ow[h1 * kHeadDim + 16 * mt + row + 8] = o[mt][3];
+    for (int t = 0; t < 2; ++t) {
+        const int d = 16 * (2 * warp + t) + row;
+        if (h0 < a.group) {
+            float* op = a.o_part + ((qbase + h0) * S + split) * kHeadDim;
+            op[d] = o[t][0];
+            op[d + 8] = o[t][2];
         }
-        if (row == 0) {
-            sm_m[warp * kMaxGroup + h0] = m_run[0];
-            sm_m[warp * kMaxGroup + h1] = m_run[1];
-            sm_l[warp * kMaxGroup + h0] = l_run[0];
-            sm_l[warp * kMaxGroup + h1] = l_run[1];
+        if (h1 < a.group) {
+            float* op = a.o_part + ((qbase + h1) * S + split) * kHeadDim;
+            op[d] = o[t][1];
+            op[d + 8] = o[t][3];
         }
     }
-    __syncthreads();
-    const int S = a.num_splits;
-    for (int idx = threadIdx.x; idx < a.group * kHeadDim; idx += kDecodeThreads) {
-        const int h = idx / kHeadDim, d = idx % kHeadDim;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + h]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kDecodeWarps; ++w) {
-                const float e = exp2f(sm_m[w * kMaxGroup + h] - M);
-                L += sm_l[w * kMaxGroup + h] * e;
-                O += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * e;
-            }
-        }
-        const int64_t qh = static_cast<int64_t>(b) * a.num_q_heads + g * a.group + h;
-        a.o_part[(qh * S + split) * kHeadDim + d] = O;
-        if (d == 0) a.ml_part[qh * S + split] = make_float2(M, L);
+    if (warp == 0 && row == 0) {
+        if (h0 < a.group) a.ml_part[(qbase + h0) * S + split] = make_float2(m_run[0], l_run[0]);
+        if (h1 < a.group) a.ml_part[(qbase + h1) * S + split] = make_float2(m_run[1], l_run[1]);
     }
 }
 
 // One warp per (request, query head); lane l owns channels 4l .. 4l+3.
-__global__ void __launch_bounds__(256) lse_combine_kernel(const float* __restrict__ o_part,
-                                                          const float2* __restrict__ ml_part, int num_splits,
-                                                          int64_t total_heads, __nv_bfloat16* __restrict__ out,
-                                                          float* __restrict__ lse) {
+// Split statistics are read one split per lane; partial outputs are loaded
+// eight splits at a time before they are combined.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(const float* __restrict__ o_part,
+                                                                      const float2* __restrict__ ml_part,
+                                                                      int num_splits, int64_t total_heads,
+                                                                      __nv_bfloat16* __restrict__ out,
+                                                                      float* __restrict__ lse) {
     const int64_t qh = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
+    pdl_wait();   // partials come from the split kernel launched just before
     if (qh >= total_heads) return;
     const float2* ml = ml_part + qh * num_splits;
-    float M = -INFINITY;
-    for (int s = lane; s < num_splits; s += 32) M = fmaxf(M, ml[s].x);
+    const float2 v0 = lane < num_splits ? ml[lane] : make_float2(-INFINITY, 0.f);
+    const float2 v1 = lane + 32 < num_splits ? ml[lane + 32] : make_float2(-INFINITY, 0.f);
+    float M = fmaxf(v0.x, v1.x);
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
+    const float e0 = M == -INFINITY ? 0.f : exp2f(v0.x - M);   // exp2(-inf) = 0 for empty splits
+    const float e1 = M == -INFINITY ? 0.f : exp2f(v1.x - M);
+    float L = v0.y * e0 + v1.y * e1;
+#pragma unroll
+    for (int s = 16; s >= 1; s >>= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
+
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = 0.f;
-    if (M != -INFINITY) {
-        for (int s = 0; s < num_splits; ++s) {
-            const float2 v = ml[s];
-            const float e = exp2f(v.x - M);   // exp2(-inf) = 0 for empty splits
-            L += v.y * e;
-            const float4 p = *reinterpret_cast<const float4*>(o_part + (qh * num_splits + s) * kHeadDim + 4 * lane);
-            acc.x += p.x * e;
-            acc.y += p.y * e;
-            acc.z += p.z * e;
-            acc.w += p.w * e;
+    const float* ob = o_part + qh * num_splits * kHeadDim + 4 * lane;
+    for (int s0 = 0; s0 < num_splits; s0 += 8) {
+        float4 p[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            p[u] = s0 + u < num_splits ? *reinterpret_cast<const float4*>(ob + (s0 + u) * kHeadDim)
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int s = s0 + u;
+            const float e = __shfl_sync(0xffffffffu, s < 32 ? e0 : e1, s & 31);
+            if (s < num_splits) {
+                acc.x += p[u].x * e;
+                acc.y += p[u].y * e;
+                acc.z += p[u].z * e;
+                acc.w += p[u].w * e;
+            }
         }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
@@ -362,14 +437,16 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     a.o_part = static_cast<float*>(workspace);
     a.ml_part = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) +
                                           ((heads * kHeadDim * sizeof(float)) + 255) / 256 * 256);
-    dim3 grid(splits, bh);
-    flash_decode_split_kernel<<<grid, kDecodeThreads, kDecodeSmem, stream>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SV_ERR_CUDA;
+    if (launch_pdl(flash_decode_split_kernel, dim3(splits, bh), dim3(kDecodeThreads), kDecodeSmem, stream, a) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
     const int64_t total_heads = static_cast<int64_t>(batch) * num_q_heads;
-    const int64_t blocks = (total_heads * 32 + 255) / 256;
-    lse_combine_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        a.o_part, a.ml_part, splits, total_heads, static_cast<__nv_bfloat16*>(out), lse);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    const int64_t blocks = (total_heads * 32 + kCombineThreads - 1) / kCombineThreads;
+    if (launch_pdl(lse_combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), 0, stream,
+                   static_cast<const float*>(a.o_part), static_cast<const float2*>(a.ml_part), splits, total_heads,
+                   static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
 }
 
 }  // namespace svq
