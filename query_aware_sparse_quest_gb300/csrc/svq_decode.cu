@@ -11,30 +11,26 @@
 // key and value, so a page is a dense (16 tokens x 128) x (128 x 8 heads)
 // product.  The token dimension is the MMA's M side: S^T = K Q^T
 // (m16n8k16, 8 k-steps) and O^T += V^T P^T (8 m-tiles of 16 channels).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "svq_common.cuh"
 
 namespace svq {
 
 SVQ_DEFINE_ERROR_WORD(read_error_decode)
 
-#ifndef SVQ_DEC_STAGES
-#define SVQ_DEC_STAGES 6
-#endif
 constexpr int kConsumers = 4;                     // consumer warps; warp w owns channels 32w .. 32w+31
 constexpr int kDecodeThreads = (kConsumers + 1) * 32;
 constexpr int kProducer = kConsumers;             // warp index of the producer
-constexpr int kStages = SVQ_DEC_STAGES;           // pages in flight per CTA
-constexpr int kRowBytes = kHeadDim * 2;           // one token's key (or value) row: 256 B
-constexpr int kRowStride = kRowBytes + 16;        // padded shared-memory row (conflict-free ldmatrix)
-constexpr int kTileBytes = kPage * kRowStride;    // one page of K (or V) for one kv head
-constexpr int kStageBytes = 2 * kTileBytes;       // K + V
-constexpr int kDecodeSmem = kStages * kStageBytes;
+constexpr int kStages = 8;                        // pages in flight per CTA (one producer lane group each)
+constexpr int kBoxBytes = kPage * 64 * 2;         // one TMA box: 16 rows x 64 channels (2 KB)
+constexpr int kStageBytes = 4 * kBoxBytes;        // K lo | K hi | V lo | V hi
+constexpr int kDecodeSmem = kStages * kStageBytes + 1024;   // + slack for 1024-byte alignment
 constexpr int kMaxSplits = 64;
 constexpr int kMinPagesPerSplit = 8;
 
 struct DecodeArgs {
-    const __nv_bfloat16* k_pool;
-    const __nv_bfloat16* v_pool;
     int64_t num_phys_pages;
     int num_kv_heads;
     const __nv_bfloat16* q;
@@ -58,19 +54,29 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-// One CTA per (split, request, kv head).  A producer warp resolves the
-// split's pages (selection list -> logical page -> physical page) and moves
-// each page's key and value rows into a kStages-deep ring with 256-byte bulk
-// copies (lane r: key row r, lane 16 + r: value row r), completing on the
-// stage's "full" mbarrier; rows past the page's fill are not copied, and the
-// value rows among them are zeroed.  Each of the four consumer warps computes
-// the page's logits S^T = K Q^T for the whole query group (the same values
-// in every warp), runs the same online softmax, and accumulates its own 32
-// output channels O^T += V^T P^T; it then arrives on the stage's "empty"
-// mbarrier so the producer can refill it.  Because every consumer holds the
-// same running max and sum, the CTA's partial needs no cross-warp merge.
-__global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
+// Byte offset of (row, 16-byte chunk) inside a 128B-swizzled TMA box whose
+// rows are 128 bytes (64 bf16): chunk c of row r sits at chunk c ^ (r & 7).
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// One CTA per (split, request, kv head).  The K and V pools are seen as 2-D
+// tensors [pages * kv heads * 16 rows][128 channels]; a page's 16 x 128 tile
+// of one kv head is two 16 x 64 TMA boxes (128-byte swizzle, so ldmatrix
+// reads are conflict-free).  Producer lane group u (lanes 4u .. 4u+3) owns
+// ring stage u and the split's pages u, u + 8, ...: after the consumers free
+// the stage, lane 4u publishes the page's valid-token count and arms the
+// stage's "full" mbarrier for 8 KB, and each of the group's four lanes moves
+// one box (K lo, K hi, V lo, V hi).  Each of the four consumer warps computes
+// the page's logits S^T = K Q^T for the whole query group (the same values in
+// every warp), runs the same online softmax and accumulates its own 32 output
+// channels O^T += V^T P^T, then arrives on the stage's "empty" mbarrier.
+// Because every consumer holds the same running max and sum, the CTA's
+// partial needs no cross-warp merge.
+__global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a,
+                                                                          const __grid_constant__ CUtensorMap tmap_k,
+                                                                          const __grid_constant__ CUtensorMap tmap_v) {
+    extern __shared__ unsigned char smem_raw[];
     __shared__ int s_valid[kStages];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -81,7 +87,9 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     const int g = bg % a.num_kv_heads;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t ring_s = smem_addr(smem);
+    const uint32_t raw_s = smem_addr(smem_raw);
+    const uint32_t ring_s = (raw_s + 1023u) & ~1023u;      // 128B swizzle wants 1024-byte aligned boxes
+    unsigned char* ring = smem_raw + (ring_s - raw_s);
     const uint32_t full0 = smem_addr(&full_bar[0]);
     const uint32_t empty0 = smem_addr(&empty_bar[0]);
 
@@ -102,6 +110,8 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     }
 
     if (warp == kProducer) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
         const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
         const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
         pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
@@ -116,73 +126,70 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const int chunk = (count + a.num_splits - 1) / a.num_splits;
         const int j0 = min(count, split * chunk);
         const int my_count = min(count, j0 + chunk) - j0;
-        // Resolve 32 pages at a time: lane l handles list position base + l.
-        int pl_phys = 0, pl_valid = 0, pl_base = -32;
-        bool failed = false;
-        int issued = 0;
-        for (int i = 0; i < my_count && !failed; ++i) {
-            if (i >= pl_base + 32) {
-                pl_base += 32;
-                const int ii = pl_base + lane;
-                pl_phys = 0;
-                pl_valid = 0;
-                if (ii < my_count) {
-                    const int j = j0 + ii;
-                    const int lp = sel_row ? sel_row[j] : j;
-                    if (lp < 0 || lp >= n) {
-                        svq_flag(SV_DEVERR_SEL_IDX);
+        const int u = lane >> 2, box = lane & 3;   // lane group u owns stage u
+        const uint32_t fb = full0 + u * 8;
+        const uint32_t eb = empty0 + u * 8;
+        const void* tmap = box < 2 ? static_cast<const void*>(&tmap_k) : static_cast<const void*>(&tmap_v);
+        const uint32_t dst = ring_s + u * kStageBytes + box * kBoxBytes;
+        // Lane l resolves list position base + l to (physical page, valid
+        // tokens); the next 32 are resolved while the current 32 are issued.
+        auto resolve = [&](int base, int& phys_out, int& valid_out) {
+            const int ii = base + lane;
+            phys_out = -1;
+            valid_out = 0;
+            if (ii < my_count) {
+                const int lp = sel_row ? sel_row[j0 + ii] : j0 + ii;
+                if (lp < 0 || lp >= n) {
+                    svq_flag(SV_DEVERR_SEL_IDX);
+                } else {
+                    const int ph = pt_row[lp];
+                    if (ph < 0 || ph >= a.num_phys_pages) {
+                        svq_flag(SV_DEVERR_PAGE_TABLE);
                     } else {
-                        const int ph = pt_row[lp];
-                        if (ph < 0 || ph >= a.num_phys_pages) {
-                            svq_flag(SV_DEVERR_PAGE_TABLE);
-                        } else {
-                            pl_phys = ph;
-                            pl_valid = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
-                        }
+                        phys_out = ph;
+                        valid_out = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
                     }
                 }
             }
-            const int stage = i % kStages;
-            if (i >= kStages) {
-                const bool ok = mbar_wait_bounded(empty0 + stage * 8, ((i / kStages) - 1) & 1);
+        };
+        int cur_phys, cur_valid, nxt_phys, nxt_valid;
+        resolve(0, cur_phys, cur_valid);
+        int last = -1;
+        bool failed = false;
+        for (int base = 0; base < my_count && !failed; base += 32) {
+            resolve(base + 32, nxt_phys, nxt_valid);
+            for (int sub = 0; sub < 32 && base + sub < my_count; sub += kStages) {
+                // Lane group u issues list position i = base + sub + u into stage u.
+                const int i = base + sub + u;
+                const int phys = __shfl_sync(0xffffffffu, cur_phys, sub + u);
+                const int valid = __shfl_sync(0xffffffffu, cur_valid, sub + u);
+                bool ok = true;
+                if (i < my_count) {
+                    if (i >= kStages) ok = mbar_wait_bounded(eb, ((i / kStages) - 1) & 1);
+                    if (ok) {
+                        if (box == 0) {
+                            s_valid[u] = phys >= 0 ? valid : 0;
+                            if (phys >= 0) mbar_arrive_expect_tx(fb, kStageBytes);
+                            else mbar_arrive(fb);
+                        }
+                        if (phys >= 0) {
+                            const int y = static_cast<int>((static_cast<int64_t>(phys) * a.num_kv_heads + g) * kPage);
+                            tma_load_2d(dst, tmap, (box & 1) * 64, y, fb);
+                        }
+                        last = i;
+                    }
+                }
                 if (__any_sync(0xffffffffu, !ok)) {
                     failed = true;
                     break;
                 }
             }
-            const int64_t phys = __shfl_sync(0xffffffffu, pl_phys, i - pl_base);
-            const int valid = __shfl_sync(0xffffffffu, pl_valid, i - pl_base);
-            unsigned char* st_ptr = smem + stage * kStageBytes;
-            if (valid < kPage) {
-                for (int c = lane; c < (kPage - valid) * 16; c += 32) {
-                    const int rr = valid + (c >> 4);
-                    *reinterpret_cast<uint4*>(st_ptr + kTileBytes + rr * kRowStride + (c & 15) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            const uint32_t fb = full0 + stage * 8;
-            if (lane == 0) {
-                s_valid[stage] = valid;
-                if (valid > 0) mbar_arrive_expect_tx(fb, static_cast<uint32_t>(valid) * 2 * kRowBytes);
-                else mbar_arrive(fb);
-            }
-            __syncwarp();
-            const int r = lane & 15;
-            if (r < valid) {
-                const int64_t row = (phys * a.num_kv_heads + g) * (kPage * kHeadDim) + r * kHeadDim;
-                bulk_copy_g2s(ring_s + stage * kStageBytes + (lane < 16 ? 0 : kTileBytes) + r * kRowStride,
-                              (lane < 16 ? a.k_pool : a.v_pool) + row, kRowBytes, fb);
-            }
-            ++issued;
+            cur_phys = nxt_phys;
+            cur_valid = nxt_valid;
         }
-        if (failed) {
-            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
-        }
-        // Every copy of this CTA lands before the CTA (and its shared memory) retires.
-        for (int p = max(0, issued - kStages); p < issued; ++p)
-            (void)mbar_wait_bounded(full0 + (p % kStages) * 8, (p / kStages) & 1);
+        if (failed) svq_flag(SV_DEVERR_TIMEOUT);
+        // This group's copies land before the CTA (and its shared memory) retires.
+        if (last >= 0) (void)mbar_wait_bounded(fb, (last / kStages) & 1);
         pdl_launch_dependents();
         return;
     }
@@ -214,30 +221,43 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     for (int t = 0; t < 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};   // heads 2 quad, 2 quad + 1 (log2 units)
     float l_run[2] = {0.f, 0.f};               // lane-partial sums
-    bool timed_out = false;
     const int mat = lane >> 3, r8 = lane & 7;
+    // Value channels of this warp: 16-byte chunks 4w .. 4w+3 of the 16 per row,
+    // i.e. box (w / 2), local chunks 4 (w % 2) .. +3.
+    const int vbox = 2 + (warp >> 1), vchunk0 = 4 * (warp & 1);
     for (int i = 0; i < my_count; ++i) {
         const int stage = i % kStages;
         const bool ok = mbar_wait_bounded(full0 + stage * 8, (i / kStages) & 1);
         if (__any_sync(0xffffffffu, !ok)) {
-            timed_out = true;
+            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
             break;
         }
-        const uint32_t ks = ring_s + stage * kStageBytes;
-        const uint32_t vs = ks + kTileBytes;
+        const uint32_t st_s = ring_s + stage * kStageBytes;
         const int valid = s_valid[stage];
+        if (valid < kPage) {
+            // Value rows past the fill hold whatever the pool holds there; zero
+            // this warp's channels of them so that P = 0 never meets a NaN.
+            // (Key rows are masked on the logits.)
+            unsigned char* vb = ring + stage * kStageBytes + vbox * kBoxBytes;
+            for (int c = lane; c < (kPage - valid) * 4; c += 32) {
+                const int rr = valid + (c >> 2);
+                *reinterpret_cast<uint4*>(vb + swz(rr, vchunk0 + (c & 3))) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
 
         // S^T (16 tokens x 8 heads) = K (16 x 128) Q^T (128 x 8), two accumulation chains.
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
         {
-            const uint32_t kaddr = ks + (r8 + 8 * (mat & 1)) * kRowStride + (mat >> 1) * 16;
+            const int krow = r8 + 8 * (mat & 1);
 #pragma unroll
-            for (int kk = 0; kk < 8; kk += 2) {
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t addr = st_s + (kk >> 2) * kBoxBytes + swz(krow, 2 * (kk & 3) + (mat >> 1));
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(kaddr + kk * 32, a0, a1, a2, a3);
-                mma_bf16_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                ldmatrix_x4(kaddr + (kk + 1) * 32, a0, a1, a2, a3);
-                mma_bf16_16816(sb, a0, a1, a2, a3, qf[kk + 1][0], qf[kk + 1][1]);
+                ldmatrix_x4(addr, a0, a1, a2, a3);
+                if (kk & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                else mma_bf16_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
             }
         }
         // Scaled logits in log2 units; tokens past the page's fill are masked.
@@ -284,19 +304,18 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
 
         // O^T (this warp's 32 channels x 8) += V^T (32 x 16) P^T (16 x 8)
         {
-            const uint32_t vaddr = vs + (r8 + 8 * (mat >> 1)) * kRowStride + (mat & 1) * 16;
+            const int vrow = r8 + 8 * (mat >> 1);
 #pragma unroll
             for (int t = 0; t < 2; ++t) {
-                const int mt = 2 * warp + t;
+                const uint32_t addr = st_s + vbox * kBoxBytes + swz(vrow, vchunk0 + 2 * t + (mat & 1));
                 uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(vaddr + mt * 32, a0, a1, a2, a3);
+                ldmatrix_x4_trans(addr, a0, a1, a2, a3);
                 mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
             }
         }
         __syncwarp();   // every lane has read the stage before it is released
         if (lane == 0) mbar_arrive(empty0 + stage * 8);
     }
-    if (timed_out && lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
 
     // Full per-head sums over the 8 lanes sharing a head.
 #pragma unroll
@@ -309,7 +328,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        const int d = 16 * (2 * warp + t) + row;
+        const int d = 32 * warp + 16 * t + row;
         if (h0 < a.group) {
             float* op = a.o_part + ((qbase + h0) * S + split) * kHeadDim;
             op[d] = o[t][0];
@@ -394,6 +413,38 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int splits) {
     return o_bytes + heads * sizeof(float2);
 }
 
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A pool bf16 [pages][kv heads][16][128] seen as a 2-D tensor
+// [pages * kv heads * 16 rows][128 channels], read in 16 x 64 boxes with the
+// 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                   const int32_t* sel_cnt, int budget_pages, float softmax_scale, void* out, float* lse,
@@ -417,9 +468,13 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     splits = max(1, min(splits, decode_max_splits(pages)));
     if (decode_workspace_bytes(batch, num_q_heads, splits) > workspace_bytes) return SV_ERR_WORKSPACE;
 
+    // TMA row coordinates are 32-bit.
+    const int64_t rows = c->num_phys_pages * c->num_kv_heads * kPage;
+    if (rows > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+    CUtensorMap tmap_k, tmap_v;
+    if (!encode_pool_map(&tmap_k, c->k_pool, rows) || !encode_pool_map(&tmap_v, c->v_pool, rows)) return SV_ERR_CUDA;
+
     DecodeArgs a;
-    a.k_pool = static_cast<const __nv_bfloat16*>(c->k_pool);
-    a.v_pool = static_cast<const __nv_bfloat16*>(c->v_pool);
     a.num_phys_pages = c->num_phys_pages;
     a.num_kv_heads = c->num_kv_heads;
     a.q = static_cast<const __nv_bfloat16*>(q);
@@ -437,8 +492,8 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     a.o_part = static_cast<float*>(workspace);
     a.ml_part = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) +
                                           ((heads * kHeadDim * sizeof(float)) + 255) / 256 * 256);
-    if (launch_pdl(flash_decode_split_kernel, dim3(splits, bh), dim3(kDecodeThreads), kDecodeSmem, stream, a) !=
-        cudaSuccess)
+    if (launch_pdl(flash_decode_split_kernel, dim3(splits, bh), dim3(kDecodeThreads), kDecodeSmem, stream, a, tmap_k,
+                   tmap_v) != cudaSuccess)
         return SV_ERR_CUDA;
     const int64_t total_heads = static_cast<int64_t>(batch) * num_q_heads;
     const int64_t blocks = (total_heads * 32 + kCombineThreads - 1) / kCombineThreads;

@@ -26,59 +26,65 @@ SVQ_DEFINE_ERROR_WORD(read_error_select)
 // 16-byte loads in flight and folds the U*HKV lane partials with a transposed
 // butterfly (one shuffle per score).
 
-#ifndef SVQ_SCORE_WARPS
-#define SVQ_SCORE_WARPS 16
+#ifndef SVQ_SCORE_CONSUMERS
+#define SVQ_SCORE_CONSUMERS 8
 #endif
-#ifndef SVQ_SCORE_STAGE_BYTES
-#define SVQ_SCORE_STAGE_BYTES 4096   // metadata bytes per ring stage (a group of pages)
+#ifndef SVQ_SCORE_RING_BYTES
+#define SVQ_SCORE_RING_BYTES (128 * 1024)
 #endif
-#ifndef SVQ_SCORE_STAGES
-#define SVQ_SCORE_STAGES 3           // stages in flight per warp
-#endif
-constexpr int kScoreWarps = SVQ_SCORE_WARPS;
-constexpr int kScoreThreads = kScoreWarps * 32;
+constexpr int kScoreConsumers = SVQ_SCORE_CONSUMERS;
+constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
+constexpr int kScoreProducer = kScoreConsumers;   // warp index of the producer
 
 template <int HKV>
 struct ScoreShape {
-    static constexpr int kPageBytes = HKV * 2 * kHeadDim * 2;              // metadata of one page, all kv heads
-    static constexpr int kGroupRaw = SVQ_SCORE_STAGE_BYTES / kPageBytes;   // pages per stage
-    static constexpr int G = kGroupRaw < 1 ? 1 : (kGroupRaw > 8 ? 8 : kGroupRaw);
-    static constexpr int kStages = SVQ_SCORE_STAGES;
-    static constexpr int kStageBytes = G * kPageBytes;
-    static constexpr int kSmemBytes = kScoreWarps * kStages * kStageBytes;
+    static constexpr int kPageBytes = HKV * 2 * kHeadDim * 2;           // metadata of one page, all kv heads
+    static constexpr int kSlotsRaw = SVQ_SCORE_RING_BYTES / kPageBytes;
+    static constexpr int kSlots = kSlotsRaw >= 128 ? 128 : (kSlotsRaw >= 64 ? 64 : 32);   // multiple of 32
+    static constexpr int kSmemBytes = kSlots * kPageBytes;
     static constexpr int L = 32 / HKV;      // lanes per kv head
-    static constexpr int kChunks = HKV;     // 16-byte chunks of a head's 512-byte row per lane
+    static constexpr int C = HKV;           // 16-byte chunks of a head's 512-byte row per lane
     static_assert(32 % HKV == 0, "kv heads per page must divide 32");
-    static_assert(32 % G == 0, "pages per stage must divide 32");
+    // Each ring slot must always be consumed by the same warp: a second warp
+    // waiting on the slot's barrier for a later phase would see that phase's
+    // parity as already complete.
+    static_assert(kSlots % kScoreConsumers == 0, "ring slots must be a multiple of the consumer warps");
 };
 
-// Each warp streams a contiguous run of one request's pages through a ring of
-// kStages stages of G pages in shared memory.  Lanes 0..G-1 each move one
-// page's metadata (all kv heads, contiguous) with a bulk copy; the copies of
-// a stage complete on one mbarrier.  Lane (j, k) = (lane / L, lane % L) owns
-// kv head j and the 16-byte chunks k, k + L, k + 2L, ... of that head's
-// 512-byte [kmin | kmax] row, so a page's score is one register accumulation
-// per lane followed by a log2(L)-level shuffle sum among the L lanes of the
-// head.  Physical page numbers are fetched 32 at a time, one batch ahead.
+// Warp-specialised streaming of page metadata.  Each CTA owns a contiguous
+// run of one request's pages.  Producer lane l handles pages l, l + 32, ...
+// of the run: it waits until the ring slot (page mod kSlots) is free, then
+// moves the page's metadata (all kv heads, contiguous) with one bulk copy
+// that completes on the slot's "full" mbarrier; the 32 lanes keep up to 32
+// copies being issued at once.  Consumer warp c scores pages c, c + C, ...:
+// lane (j, k) = (lane / L, lane % L) owns kv head j and the 16-byte chunks
+// k, k + L, ... of that head's 512-byte [kmin | kmax] row, so a page's score
+// is one register accumulation per lane plus a log2(L)-level shuffle sum;
+// the warp then releases the slot on its "empty" mbarrier.
 template <int HKV>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const __nv_bfloat16* __restrict__ meta, int64_t num_phys_pages, const __nv_bfloat16* __restrict__ q,
     int group, const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens, int max_pages,
     int pages_per_cta, float* __restrict__ scores) {
     using S = ScoreShape<HKV>;
-    constexpr int kStages = S::kStages, G = S::G, L = S::L, C = S::kChunks;
+    constexpr int kSlots = S::kSlots, L = S::L, C = S::C;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ float coef[HKV][2][kHeadDim];   // [j][0] = Qn (pairs kmin), [j][1] = Qp (pairs kmax)
-    __shared__ __align__(8) uint64_t bars[kScoreWarps][kStages];
+    __shared__ __align__(8) uint64_t full_bar[kSlots];
+    __shared__ __align__(8) uint64_t empty_bar[kSlots];
+    __shared__ unsigned char slot_ok[kSlots];
 
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
-    const int hj = lane / L;        // kv head of this lane
-    const int hk = lane % L;        // first chunk of this lane
+    const uint32_t full0 = smem_addr(&full_bar[0]);
+    const uint32_t empty0 = smem_addr(&empty_bar[0]);
 
-    if (lane == 0) {
-        for (int st = 0; st < kStages; ++st) mbar_init(smem_addr(&bars[warp][st]), 1);
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kSlots; ++st) {
+            mbar_init(full0 + st * 8, 1);
+            mbar_init(empty0 + st * 8, 1);
+        }
         mbar_init_fence();
     }
     // Fold the group's query heads into Qp / Qn (q is an input of the step).
@@ -94,7 +100,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         coef[j][0][ch] = qn;
         coef[j][1][ch] = qp;
     }
-    pdl_wait();   // metadata may come from an append launched just before
     __syncthreads();
 
     const int len = seq_lens[b];
@@ -104,135 +109,88 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         n = len < 1 ? 0 : max_pages;
     }
     const int cta_begin = blockIdx.x * pages_per_cta;
-    const int cta_end = min(n, cta_begin + pages_per_cta);
-    const int span = max(0, cta_end - cta_begin);
-    const int per_warp = (span + kScoreWarps - 1) / kScoreWarps;
-    const int w_begin = cta_begin + min(span, warp * per_warp);
-    const int count = max(0, min(cta_end, w_begin + per_warp) - w_begin);
-    const int n_groups = (count + G - 1) / G;
+    const int span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
+    // Metadata may come from an append launched just before, and the previous
+    // step's top-K may still read the score buffer.
+    pdl_wait();
 
-    // Chunk t of this lane is chunk hk + L t of the head's row: kmin channels
-    // for chunks < 16, kmax channels for chunks >= 16.
+    if (warp == kScoreProducer) {
+        const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
+        const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(meta);
+        const uint32_t ring_s = smem_addr(ring);
+        int issued_last = -1;   // highest page this lane issued
+        bool failed = false;
+        int nxt = lane < span ? pt_row[lane] : 0;
+        for (int p = lane; p < span; p += 32) {
+            const int phys = nxt;
+            if (p + 32 < span) nxt = pt_row[p + 32];
+            const int slot = p % kSlots;
+            if (p >= kSlots && !mbar_wait_bounded(empty0 + slot * 8, ((p / kSlots) - 1) & 1)) {
+                failed = true;
+                break;
+            }
+            const uint32_t fb = full0 + slot * 8;
+            const bool ok = static_cast<uint32_t>(phys) < static_cast<uint64_t>(num_phys_pages);
+            slot_ok[slot] = ok ? 1 : 0;
+            if (ok) {
+                mbar_arrive_expect_tx(fb, S::kPageBytes);
+                bulk_copy_g2s(ring_s + slot * S::kPageBytes, meta_bytes + static_cast<int64_t>(phys) * S::kPageBytes,
+                              S::kPageBytes, fb);
+            } else {
+                svq_flag(SV_DEVERR_PAGE_TABLE);
+                mbar_arrive(fb);
+            }
+            issued_last = p;
+        }
+        if (failed) svq_flag(SV_DEVERR_TIMEOUT);
+        // This lane's copies land before the CTA (and its shared memory) retires.
+        for (int p = issued_last; p >= 0 && p > issued_last - kSlots; p -= 32)
+            (void)mbar_wait_bounded(full0 + (p % kSlots) * 8, (p / kSlots) & 1);
+        pdl_launch_dependents();
+        return;
+    }
+
+    // ---------------- consumer warps
+    const int hj = lane / L;        // kv head of this lane
+    const int hk = lane % L;        // first chunk of this lane
     float c[C][8];
 #pragma unroll
     for (int t = 0; t < C; ++t) {
-        const int chunk = hk + L * t;
+        const int chunk = hk + L * t;   // chunks < 16 hold kmin channels, >= 16 kmax
 #pragma unroll
         for (int i = 0; i < 8; ++i) c[t][i] = coef[hj][chunk >> 4][(chunk & 15) * 8 + i];
     }
-
-    const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + w_begin;
-    float* score_row = scores + (static_cast<int64_t>(b) * HKV + hj) * max_pages + w_begin;
-    const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(meta);
-    const unsigned char* ring_w = ring + warp * (kStages * S::kStageBytes);
-    const uint32_t ring_s = smem_addr(ring_w);
-    const uint32_t bar0 = smem_addr(&bars[warp][0]);
-
-    auto load_pt = [&](int base) -> int {
-        const int p = base + lane;
-        int v = p < count ? pt_row[p] : -1;
-        if (p < count && static_cast<uint32_t>(v) >= static_cast<uint64_t>(num_phys_pages)) {
-            svq_flag(SV_DEVERR_PAGE_TABLE);
-            v = -1;
-        }
-        return v;
-    };
-    int pt_base = 0;
-    int pt_cur = load_pt(0);
-    int pt_nxt = load_pt(32);
-    uint32_t stage_ok[kStages];   // bit u: page u of the stage is real (uniform across the warp)
-#pragma unroll
-    for (int st = 0; st < kStages; ++st) stage_ok[st] = 0u;
-    // Issues group gi (warp-uniform, increasing) into ring stage `stage`.
-    auto issue = [&](int gi, int stage) -> uint32_t {
-        const int p0 = gi * G;
-        if (p0 >= pt_base + 32) {   // G divides 32, so a group never straddles two batches
-            pt_base += 32;
-            pt_cur = pt_nxt;
-            pt_nxt = load_pt(pt_base + 32);
-        }
-        const int mine = __shfl_sync(0xffffffffu, pt_cur, (p0 - pt_base + (lane % G)) & 31);
-        const uint32_t ok = __ballot_sync(0xffffffffu, lane < G && mine >= 0) & ((1u << G) - 1u);
-        const uint32_t bar = bar0 + stage * 8;
-        if (lane == 0) {
-            if (ok) mbar_arrive_expect_tx(bar, __popc(ok) * S::kPageBytes);
-            else mbar_arrive(bar);
-        }
-        __syncwarp();
-        if (lane < G && mine >= 0)
-            bulk_copy_g2s(ring_s + stage * S::kStageBytes + lane * S::kPageBytes,
-                          meta_bytes + static_cast<int64_t>(mine) * S::kPageBytes, S::kPageBytes, bar);
-        return ok;
-    };
-
-    __syncwarp();   // barriers initialised before any use
-    int issued = 0;
-#pragma unroll
-    for (int st = 0; st < kStages; ++st)
-        if (st < n_groups) stage_ok[st] = issue(st, st), ++issued;
-    bool timed_out = false;
-    int consumed = 0;
-    const unsigned char* lane_base = ring_w + hj * 512 + hk * 16;
-    for (int gi = 0; gi < n_groups; ++gi) {
-        const int stage = gi % kStages;
-        const bool ok = mbar_wait_bounded(bar0 + stage * 8, (gi / kStages) & 1);
-        if (__any_sync(0xffffffffu, !ok)) {
-            timed_out = true;
+    float* score_row = scores + (static_cast<int64_t>(b) * HKV + hj) * max_pages + cta_begin;
+    const unsigned char* lane_base = ring + hj * 512 + hk * 16;
+    for (int p = warp; p < span; p += kScoreConsumers) {
+        const int slot = p % kSlots;
+        const bool okw = mbar_wait_bounded(full0 + slot * 8, (p / kSlots) & 1);
+        if (__any_sync(0xffffffffu, !okw)) {
+            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
             break;
         }
-        consumed = gi + 1;
-        uint32_t okm = 0;
+        uint4 w[C];
 #pragma unroll
-        for (int st = 0; st < kStages; ++st) okm = st == stage ? stage_ok[st] : okm;
-        float acc[G];
+        for (int t = 0; t < C; ++t)
+            w[t] = *reinterpret_cast<const uint4*>(lane_base + slot * S::kPageBytes + t * L * 16);
+        const bool real = slot_ok[slot] != 0;
+        __syncwarp();   // every lane has read the slot before it is released
+        if (lane == 0) mbar_arrive(empty0 + slot * 8);
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int u = 0; u < G; ++u) {
-            uint4 w[C];
+        for (int t = 0; t < C; ++t) {
+            const uint32_t x[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
 #pragma unroll
-            for (int t = 0; t < C; ++t)
-                w[t] = *reinterpret_cast<const uint4*>(lane_base + stage * S::kStageBytes + u * S::kPageBytes +
-                                                       t * L * 16);
-            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                const uint32_t x[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    a0 = fmaf(c[t][2 * e], bf16lo(x[e]), a0);
-                    a1 = fmaf(c[t][2 * e + 1], bf16hi(x[e]), a1);
-                }
+            for (int e = 0; e < 4; ++e) {
+                a0 = fmaf(c[t][2 * e], bf16lo(x[e]), a0);
+                a1 = fmaf(c[t][2 * e + 1], bf16hi(x[e]), a1);
             }
-            acc[u] = (okm & (1u << u)) ? a0 + a1 : 0.f;
         }
-        __syncwarp();   // every lane has read the stage before it is refilled
-        if (gi + kStages < n_groups) {
-            const uint32_t nok = issue(gi + kStages, stage);
+        float acc = real ? a0 + a1 : 0.f;
 #pragma unroll
-            for (int st = 0; st < kStages; ++st) stage_ok[st] = st == stage ? nok : stage_ok[st];
-            ++issued;
-        }
-#pragma unroll
-        for (int u = 0; u < G; ++u) {
-#pragma unroll
-            for (int m = 1; m < L; m <<= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], m);
-        }
-        if (hk < G) {
-            // Lane (j, u) writes page u's score for head j.
-            float v = acc[0];
-#pragma unroll
-            for (int u = 1; u < G; ++u) v = hk == u ? acc[u] : v;
-            const int p = gi * G + hk;
-            if (p < count) score_row[p] = v;
-        }
+        for (int m = 1; m < L; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+        if (hk == 0) score_row[p] = acc;
     }
-    if (timed_out) {
-        // Give the copies this warp still has in flight a bounded chance to land
-        // before the CTA's shared memory is released.
-        if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
-        for (int gi = consumed; gi < issued; ++gi)
-            (void)mbar_wait_bounded(bar0 + (gi % kStages) * 8, (gi / kStages) & 1);
-    }
-    pdl_launch_dependents();
 }
 
 template <int HKV>
@@ -249,10 +207,9 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
             return SV_ERR_CUDA;
         if (dev < 64) attr_set[dev] = true;
     }
-    // One CTA per SM over the (batch x max_pages) page grid, whole warps of pages.
+    // One CTA per SM over the (batch x max_pages) page grid.
     int64_t ppc = (static_cast<int64_t>(batch) * max_pages + sm_count - 1) / sm_count;
-    ppc = ((ppc + kScoreWarps - 1) / kScoreWarps) * kScoreWarps;
-    if (ppc < kScoreWarps) ppc = kScoreWarps;
+    if (ppc < 32) ppc = 32;
     const int ctas = ceil_div(max_pages, ppc);
     const cudaError_t e = launch_pdl(score_pages_kernel<HKV>, dim3(ctas, batch), dim3(kScoreThreads),
                                      S::kSmemBytes, stream, static_cast<const __nv_bfloat16*>(c->meta),
@@ -289,18 +246,23 @@ int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_
 // A block-wide scan over contiguous index segments then emits, in ascending
 // index order, every page above T and the lowest-indexed pages equal to T.
 
-constexpr int kTopkThreads = 1024;
+#ifndef SVQ_TOPK_THREADS
+#define SVQ_TOPK_THREADS 1024
+#endif
+constexpr int kTopkThreads = SVQ_TOPK_THREADS;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kRadixBins = 2048;
+constexpr int kBinsPerThread = kRadixBins / kTopkThreads;
 constexpr int kLoadItems = 8;
 constexpr int kCandCap = 256;
+static_assert(kRadixBins % kTopkThreads == 0 && kTopkWarps <= 32, "top-K block shape");
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide inclusive scan of one value per thread (1024 threads).
+// Block-wide inclusive scan of one value per thread.
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -311,13 +273,13 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
     if (warp == 0) {
-        uint32_t t = warp_tot[lane];
+        uint32_t t = lane < kTopkWarps ? warp_tot[lane] : 0u;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t x = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o) t += x;
         }
-        warp_tot[lane] = t;
+        if (lane < kTopkWarps) warp_tot[lane] = t;
     }
     __syncthreads();
     const uint32_t add = warp > 0 ? warp_tot[warp - 1] : 0u;
@@ -330,26 +292,37 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
 __device__ __forceinline__ void find_bin_from_top(const uint32_t* hist, uint32_t remaining, uint32_t* warp_tot,
                                                   uint32_t* s_bin, uint32_t* s_rem) {
     const int tid = threadIdx.x;
-    const uint32_t hi_bin = kRadixBins - 1 - 2 * tid;   // thread t owns bins 2047-2t, 2046-2t
-    const uint32_t c0 = hist[hi_bin], c1 = hist[hi_bin - 1];
-    const uint32_t incl = block_inclusive_scan(c0 + c1, warp_tot);
-    const uint32_t excl = incl - c0 - c1;
-    if (excl < remaining && remaining <= excl + c0) {
-        *s_bin = hi_bin;
-        *s_rem = remaining - excl;
-    } else if (excl + c0 < remaining && remaining <= excl + c0 + c1) {
-        *s_bin = hi_bin - 1;
-        *s_rem = remaining - excl - c0;
+    // Thread t owns kBinsPerThread consecutive bins counted down from the top.
+    const uint32_t top = kRadixBins - 1 - kBinsPerThread * tid;
+    uint32_t cnt[kBinsPerThread];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) {
+        cnt[i] = hist[top - i];
+        sum += cnt[i];
+    }
+    uint32_t before = block_inclusive_scan(sum, warp_tot) - sum;   // keys in strictly higher bins
+#pragma unroll
+    for (int i = 0; i < kBinsPerThread; ++i) {
+        if (before < remaining && remaining <= before + cnt[i]) {
+            *s_bin = top - i;
+            *s_rem = remaining - before;
+        }
+        before += cnt[i];
     }
     __syncthreads();
 }
 
+// Keys live in registers: thread t holds the ITEMS consecutive pages
+// [ITEMS t, ITEMS t + ITEMS) of the row (n <= ITEMS * kTopkThreads), so the
+// final compaction emits in ascending page order from per-thread bit masks.
+template <int ITEMS>
 __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* __restrict__ scores,
                                                                   const int32_t* __restrict__ seq_lens,
                                                                   int num_kv_heads, int max_pages, int K,
                                                                   int32_t* __restrict__ sel_idx,
                                                                   int32_t* __restrict__ sel_cnt) {
-    extern __shared__ uint32_t keys[];   // [max_pages]
+    static_assert(ITEMS <= 32, "selection masks are 32 bits");
     __shared__ uint32_t hist[kRadixBins];
     __shared__ uint32_t warp_tot[kTopkWarps];
     __shared__ uint32_t warp_lo[kTopkWarps], warp_hi[kTopkWarps];
@@ -370,6 +343,8 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     }
     const int m = min(K, n);
     int32_t* out = sel_idx + static_cast<int64_t>(bg) * K;
+    for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
+    if (tid == 0) s_cand = 0u;
     pdl_wait();   // scores come from the scoring kernel launched just before
     if (n <= K) {
         for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
@@ -378,25 +353,28 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         return;
     }
 
-    // 1. keys (all loads of a round issued before any use), min and max.
+    // 1. this thread's keys, min and max.
     const float* row = scores + static_cast<int64_t>(bg) * max_pages;
-    uint32_t lo = 0xffffffffu, hi = 0u;
-    for (int base = 0; base < n; base += kTopkThreads * kLoadItems) {
-        float f[kLoadItems];
+    const int i0 = ITEMS * tid;
+    float f[ITEMS];
+    if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && i0 + ITEMS <= n) {
 #pragma unroll
-        for (int r = 0; r < kLoadItems; ++r) {
-            const int i = base + r * kTopkThreads + tid;
-            f[r] = i < n ? row[i] : 0.f;
+        for (int e = 0; e < ITEMS; e += 4) {
+            const float4 v = *reinterpret_cast<const float4*>(row + i0 + e);
+            f[e] = v.x; f[e + 1] = v.y; f[e + 2] = v.z; f[e + 3] = v.w;
         }
+    } else {
 #pragma unroll
-        for (int r = 0; r < kLoadItems; ++r) {
-            const int i = base + r * kTopkThreads + tid;
-            if (i < n) {
-                const uint32_t k = order_key(f[r]);
-                keys[i] = k;
-                lo = min(lo, k);
-                hi = max(hi, k);
-            }
+        for (int e = 0; e < ITEMS; ++e) f[e] = i0 + e < n ? row[i0 + e] : 0.f;
+    }
+    uint32_t key[ITEMS];
+    uint32_t lo = 0xffffffffu, hi = 0u;
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) {
+        key[e] = order_key(f[e]);
+        if (i0 + e < n) {
+            lo = min(lo, key[e]);
+            hi = max(hi, key[e]);
         }
     }
     lo = __reduce_min_sync(0xffffffffu, lo);
@@ -405,12 +383,10 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         warp_lo[warp] = lo;
         warp_hi[warp] = hi;
     }
-    for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
-    if (tid == 0) s_cand = 0u;
     __syncthreads();
     if (warp == 0) {
-        lo = __reduce_min_sync(0xffffffffu, warp_lo[lane]);
-        hi = __reduce_max_sync(0xffffffffu, warp_hi[lane]);
+        lo = __reduce_min_sync(0xffffffffu, lane < kTopkWarps ? warp_lo[lane] : 0xffffffffu);
+        hi = __reduce_max_sync(0xffffffffu, lane < kTopkWarps ? warp_hi[lane] : 0u);
         if (lane == 0) {
             const uint32_t range = hi - lo;
             const int bits = range == 0 ? 0 : 32 - __clz(range);   // range < 2^bits
@@ -423,39 +399,43 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     const uint32_t shift = s_shift;
 
     // 2. histogram of (key - lo) >> shift; bin of the m-th best key.
-    for (int i = tid; i < n; i += kTopkThreads) atomicAdd(&hist[(keys[i] - lo) >> shift], 1u);
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e)
+        if (i0 + e < n) atomicAdd(&hist[(key[e] - lo) >> shift], 1u);
     __syncthreads();
     find_bin_from_top(hist, static_cast<uint32_t>(m), warp_tot, &s_bin, &s_rem);
     const uint32_t bstar = s_bin, need = s_rem;
     uint32_t T, take;
     if (hist[bstar] <= kCandCap) {
         // 3a. exact rank of each key of bin b* among the others.
-        for (int i = tid; i < n; i += kTopkThreads) {
-            const uint32_t k = keys[i];
-            if (((k - lo) >> shift) == bstar) {
+#pragma unroll
+        for (int e = 0; e < ITEMS; ++e) {
+            if (i0 + e < n && ((key[e] - lo) >> shift) == bstar) {
                 const uint32_t pos = atomicAdd(&s_cand, 1u);
-                cand_key[pos] = k;
-                cand_idx[pos] = i;
-            }
-        }
-        __syncthreads();
-        const int nc = static_cast<int>(s_cand);
-        if (tid < nc) {
-            const uint32_t k = cand_key[tid];
-            const int idx = cand_idx[tid];
-            uint32_t rank = 0;
-            for (int j = 0; j < nc; ++j) {
-                const uint32_t kj = cand_key[j];
-                rank += (kj > k) || (kj == k && cand_idx[j] < idx);
-            }
-            if (rank == need - 1) {
-                s_T = k;
-                s_Tidx = idx;
+                cand_key[pos] = key[e];
+                cand_idx[pos] = i0 + e;
             }
         }
         if (tid == 0) s_take = 0u;
         __syncthreads();
-        if (tid < nc && cand_key[tid] == s_T && cand_idx[tid] <= s_Tidx) atomicAdd(&s_take, 1u);
+        const int nc = static_cast<int>(s_cand);
+        uint32_t my_k = 0;
+        int my_i = 0;
+        if (tid < nc) {
+            my_k = cand_key[tid];
+            my_i = cand_idx[tid];
+            uint32_t rank = 0;
+            for (int j = 0; j < nc; ++j) {
+                const uint32_t kj = cand_key[j];
+                rank += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
+            }
+            if (rank == need - 1) {
+                s_T = my_k;
+                s_Tidx = my_i;
+            }
+        }
+        __syncthreads();
+        if (tid < nc && my_k == s_T && my_i <= s_Tidx) atomicAdd(&s_take, 1u);
         __syncthreads();
         T = s_T;
         take = s_take;
@@ -472,10 +452,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
             __syncthreads();
             for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
             __syncthreads();
-            for (int i = tid; i < n; i += kTopkThreads) {
-                const uint32_t k = keys[i];
-                if ((k & hi_mask) == prefix) atomicAdd(&hist[(k >> sh) & (nbins - 1u)], 1u);
-            }
+#pragma unroll
+            for (int e = 0; e < ITEMS; ++e)
+                if (i0 + e < n && (key[e] & hi_mask) == prefix) atomicAdd(&hist[(key[e] >> sh) & (nbins - 1u)], 1u);
             __syncthreads();
             find_bin_from_top(hist, remaining, warp_tot, &s_bin, &s_rem);
             prefix |= s_bin << sh;
@@ -485,30 +464,33 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         take = remaining;
     }
 
-    // 4. ordered compaction over contiguous index segments.
-    const int seg = (n + kTopkThreads - 1) / kTopkThreads;
-    const int s0 = min(n, tid * seg), s1 = min(n, s0 + seg);
-    uint32_t gt = 0, eq = 0;
-    for (int i = s0; i < s1; ++i) {
-        const uint32_t k = keys[i];
-        gt += k > T;
-        eq += k == T;
+    // 4. ordered compaction: every key above T, and the `take` lowest-indexed keys equal to T.
+    uint32_t gt_mask = 0, eq_mask = 0;
+#pragma unroll
+    for (int e = 0; e < ITEMS; ++e) {
+        if (i0 + e < n) {
+            gt_mask |= (key[e] > T ? 1u : 0u) << e;
+            eq_mask |= (key[e] == T ? 1u : 0u) << e;
+        }
     }
+    const uint32_t gt = __popc(gt_mask), eq = __popc(eq_mask);
     const uint32_t packed = (gt << 16) | eq;   // n <= 32768 keeps both halves in 16 bits
     const uint32_t excl = block_inclusive_scan(packed, warp_tot) - packed;
-    uint32_t eq_seen = excl & 0xffffu;
-    uint32_t pos = (excl >> 16) + min(eq_seen, take);
-    for (int i = s0; i < s1; ++i) {
-        const uint32_t k = keys[i];
-        bool sel = k > T;
-        if (k == T) {
-            sel = eq_seen < take;
-            ++eq_seen;
-        }
-        if (sel) {
-            if (pos < static_cast<uint32_t>(m)) out[pos] = i;
-            ++pos;
-        }
+    const uint32_t eq_before = excl & 0xffffu;
+    uint32_t sel_mask = gt_mask;
+    uint32_t eq_take = take > eq_before ? min(take - eq_before, eq) : 0u;
+    uint32_t eqm = eq_mask;
+    while (eq_take--) {
+        const uint32_t low = eqm & (0u - eqm);
+        sel_mask |= low;
+        eqm ^= low;
+    }
+    uint32_t pos = (excl >> 16) + min(eq_before, take);
+    while (sel_mask) {
+        const int e = __ffs(sel_mask) - 1;
+        sel_mask &= sel_mask - 1u;
+        if (pos < static_cast<uint32_t>(m)) out[pos] = i0 + e;
+        ++pos;
     }
     for (int i = m + tid; i < K; i += kTopkThreads) out[i] = -1;
     if (tid == 0) sel_cnt[bg] = m;
@@ -517,15 +499,19 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
 
 int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
                 int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(max_pages) * sizeof(uint32_t);
-    if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(topk_pages_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return SV_ERR_CUDA;
-    }
-    const cudaError_t e = launch_pdl(topk_pages_kernel, dim3(batch * num_kv_heads), dim3(kTopkThreads), smem,
-                                     stream, scores, seq_lens, num_kv_heads, max_pages, budget_pages, sel_idx,
-                                     sel_cnt);
+    cudaError_t e;
+    const dim3 grid(batch * num_kv_heads), block(kTopkThreads);
+    if (max_pages <= 8 * kTopkThreads)
+        e = launch_pdl(topk_pages_kernel<8>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
+    else if (max_pages <= 16 * kTopkThreads)
+        e = launch_pdl(topk_pages_kernel<16>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
+    else if (max_pages <= 32 * kTopkThreads)
+        e = launch_pdl(topk_pages_kernel<32>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
+    else
+        return SV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
