@@ -24,6 +24,7 @@ constexpr int kConsumers = 4;                     // consumer warps; warp w owns
 constexpr int kDecodeThreads = (kConsumers + 1) * 32;
 constexpr int kProducer = kConsumers;             // warp index of the producer
 constexpr int kStages = 8;                        // pages in flight per CTA (one producer lane group each)
+static_assert(kStages % kConsumers == 0, "each ring stage must belong to one consumer warp");
 constexpr int kBoxBytes = kPage * 64 * 2;         // one TMA box: 16 rows x 64 channels (2 KB)
 constexpr int kStageBytes = 4 * kBoxBytes;        // K lo | K hi | V lo | V hi
 constexpr int kDecodeSmem = kStages * kStageBytes + 1024;   // + slack for 1024-byte alignment
@@ -96,7 +97,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     if (threadIdx.x == 0) {
         for (int st = 0; st < kStages; ++st) {
             mbar_init(full0 + st * 8, 1);
-            mbar_init(empty0 + st * 8, kConsumers);
+            mbar_init(empty0 + st * 8, 1);   // stage s is consumed by warp s % kConsumers alone
         }
         mbar_init_fence();
     }
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         return;
     }
 
-    // ---------------- consumer warps
+    // ---------------- consumer warps: warp w takes the split's pages w, w + 4, ...
     const int quad = lane & 3;      // column pair of the accumulator fragments
     const int row = lane >> 2;      // row of the accumulator fragments
     // Q^T fragments (B operand): head `row` of the group, channels 16kk + 2 quad (+8).
@@ -216,16 +217,15 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     const int j0 = min(count, split * chunk);
     const int my_count = min(count, j0 + chunk) - j0;
 
-    float o[2][4];
+    float o[8][4];
 #pragma unroll
-    for (int t = 0; t < 2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};   // heads 2 quad, 2 quad + 1 (log2 units)
     float l_run[2] = {0.f, 0.f};               // lane-partial sums
     const int mat = lane >> 3, r8 = lane & 7;
-    // Value channels of this warp: 16-byte chunks 4w .. 4w+3 of the 16 per row,
-    // i.e. box (w / 2), local chunks 4 (w % 2) .. +3.
-    const int vbox = 2 + (warp >> 1), vchunk0 = 4 * (warp & 1);
-    for (int i = 0; i < my_count; ++i) {
+    const int krow = r8 + 8 * (mat & 1);       // ldmatrix row of the key tile
+    const int vrow = r8 + 8 * (mat >> 1);      // ldmatrix row of the value tile
+    for (int i = warp; i < my_count; i += kConsumers) {
         const int stage = i % kStages;
         const bool ok = mbar_wait_bounded(full0 + stage * 8, (i / kStages) & 1);
         if (__any_sync(0xffffffffu, !ok)) {
@@ -236,12 +236,12 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const int valid = s_valid[stage];
         if (valid < kPage) {
             // Value rows past the fill hold whatever the pool holds there; zero
-            // this warp's channels of them so that P = 0 never meets a NaN.
-            // (Key rows are masked on the logits.)
-            unsigned char* vb = ring + stage * kStageBytes + vbox * kBoxBytes;
-            for (int c = lane; c < (kPage - valid) * 4; c += 32) {
-                const int rr = valid + (c >> 2);
-                *reinterpret_cast<uint4*>(vb + swz(rr, vchunk0 + (c & 3))) = make_uint4(0u, 0u, 0u, 0u);
+            // them so that P = 0 never meets a NaN.  (Key rows are masked on
+            // the logits.)
+            unsigned char* vb = ring + stage * kStageBytes + 2 * kBoxBytes;
+            for (int c = lane; c < (kPage - valid) * 16; c += 32) {
+                const int rr = valid + (c >> 4);
+                *reinterpret_cast<uint4*>(vb + (c & 8 ? kBoxBytes : 0) + swz(rr, c & 7)) = make_uint4(0u, 0u, 0u, 0u);
             }
             fence_proxy_async_smem();
             __syncwarp();
@@ -249,16 +249,13 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
 
         // S^T (16 tokens x 8 heads) = K (16 x 128) Q^T (128 x 8), two accumulation chains.
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            const int krow = r8 + 8 * (mat & 1);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t addr = st_s + (kk >> 2) * kBoxBytes + swz(krow, 2 * (kk & 3) + (mat >> 1));
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(addr, a0, a1, a2, a3);
-                if (kk & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                else mma_bf16_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-            }
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t addr = st_s + (kk >> 2) * kBoxBytes + swz(krow, 2 * (kk & 3) + (mat >> 1));
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4(addr, a0, a1, a2, a3);
+            if (kk & 1) mma_bf16_16816(sb, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            else mma_bf16_16816(sa, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
         }
         // Scaled logits in log2 units; tokens past the page's fill are masked.
         const float x0 = row < valid ? (sa[0] + sb[0]) * a.scale_log2 : -INFINITY;       // token row,   head 2q
@@ -282,11 +279,11 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         l_run[0] = l_run[0] * alpha0 + p0 + p2;
         l_run[1] = l_run[1] * alpha1 + p1 + p3;
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-            o[t][0] *= alpha0;
-            o[t][1] *= alpha1;
-            o[t][2] *= alpha0;
-            o[t][3] *= alpha1;
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= alpha0;
+            o[mt][1] *= alpha1;
+            o[mt][2] *= alpha0;
+            o[mt][3] *= alpha1;
         }
 
         // P^T as the B operand: lane needs P[token 2 quad + {0,1} (+8)][head row].
@@ -302,16 +299,13 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const uint32_t pb0 = __byte_perm(lo0, lo1, selector);
         const uint32_t pb1 = __byte_perm(hi0, hi1, selector);
 
-        // O^T (this warp's 32 channels x 8) += V^T (32 x 16) P^T (16 x 8)
-        {
-            const int vrow = r8 + 8 * (mat >> 1);
+        // O^T (128 channels x 8) += V^T (128 x 16) P^T (16 x 8)
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const uint32_t addr = st_s + vbox * kBoxBytes + swz(vrow, vchunk0 + 2 * t + (mat & 1));
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4_trans(addr, a0, a1, a2, a3);
-                mma_bf16_16816(o[t], a0, a1, a2, a3, pb0, pb1);
-            }
+        for (int mt = 0; mt < 8; ++mt) {
+            const uint32_t addr = st_s + (2 + (mt >> 2)) * kBoxBytes + swz(vrow, 2 * (mt & 3) + (mat & 1));
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(addr, a0, a1, a2, a3);
+            mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
         }
         __syncwarp();   // every lane has read the stage before it is released
         if (lane == 0) mbar_arrive(empty0 + stage * 8);
@@ -323,26 +317,49 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], s);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], s);
     }
-    const int S = a.num_splits;
-    const int h0 = 2 * quad, h1 = 2 * quad + 1;
-    const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
+
+    // Merge the consumer warps through shared memory (the ring is idle: every
+    // page of this CTA has been consumed, so no copy is in flight).
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+    float* sm_o = reinterpret_cast<float*>(ring);                   // [warp][8][128]
+    float* sm_m = sm_o + kConsumers * kMaxGroup * kHeadDim;         // [warp][8]
+    float* sm_l = sm_m + kConsumers * kMaxGroup;                    // [warp][8]
+    {
+        float* ow = sm_o + warp * kMaxGroup * kHeadDim;
+        const int h0 = 2 * quad, h1 = 2 * quad + 1;
 #pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        const int d = 32 * warp + 16 * t + row;
-        if (h0 < a.group) {
-            float* op = a.o_part + ((qbase + h0) * S + split) * kHeadDim;
-            op[d] = o[t][0];
-            op[d + 8] = o[t][2];
+        for (int mt = 0; mt < 8; ++mt) {
+            ow[h0 * kHeadDim + 16 * mt + row] = o[mt][0];
+            ow[h1 * kHeadDim + 16 * mt + row] = o[mt][1];
+            ow[h0 * kHeadDim + 16 * mt + row + 8] = o[mt][2];
+            ow[h1 * kHeadDim + 16 * mt + row + 8] = o[mt][3];
         }
-        if (h1 < a.group) {
-            float* op = a.o_part + ((qbase + h1) * S + split) * kHeadDim;
-            op[d] = o[t][1];
-            op[d + 8] = o[t][3];
+        if (row == 0) {
+            sm_m[warp * kMaxGroup + h0] = m_run[0];
+            sm_m[warp * kMaxGroup + h1] = m_run[1];
+            sm_l[warp * kMaxGroup + h0] = l_run[0];
+            sm_l[warp * kMaxGroup + h1] = l_run[1];
         }
     }
-    if (warp == 0 && row == 0) {
-        if (h0 < a.group) a.ml_part[(qbase + h0) * S + split] = make_float2(m_run[0], l_run[0]);
-        if (h1 < a.group) a.ml_part[(qbase + h1) * S + split] = make_float2(m_run[1], l_run[1]);
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers * 32) : "memory");
+    const int S = a.num_splits;
+    const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
+    for (int idx = threadIdx.x; idx < a.group * kHeadDim; idx += kConsumers * 32) {
+        const int h = idx / kHeadDim, d = idx % kHeadDim;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float e = fast_exp2(sm_m[w * kMaxGroup + h] - M);
+                L += sm_l[w * kMaxGroup + h] * e;
+                O += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * e;
+            }
+        }
+        a.o_part[((qbase + h) * S + split) * kHeadDim + d] = O;
+        if (d == 0) a.ml_part[(qbase + h) * S + split] = make_float2(M, L);
     }
 }
 

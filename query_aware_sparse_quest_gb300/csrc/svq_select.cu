@@ -40,7 +40,7 @@ template <int HKV>
 struct ScoreShape {
     static constexpr int kPageBytes = HKV * 2 * kHeadDim * 2;           // metadata of one page, all kv heads
     static constexpr int kSlotsRaw = SVQ_SCORE_RING_BYTES / kPageBytes;
-    static constexpr int kSlots = kSlotsRaw >= 128 ? 128 : (kSlotsRaw >= 64 ? 64 : 32);   // multiple of 32
+    static constexpr int kSlots = kSlotsRaw >= 128 ? 128 : (kSlotsRaw < 32 ? 32 : kSlotsRaw / 32 * 32);   // multiple of 32
     static constexpr int kSmemBytes = kSlots * kPageBytes;
     static constexpr int L = 32 / HKV;      // lanes per kv head
     static constexpr int C = HKV;           // 16-byte chunks of a head's 512-byte row per lane
@@ -73,6 +73,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     __shared__ __align__(8) uint64_t full_bar[kSlots];
     __shared__ __align__(8) uint64_t empty_bar[kSlots];
     __shared__ unsigned char slot_ok[kSlots];
+    __shared__ __align__(16) __nv_bfloat16 qstage[HKV * kMaxGroup * kHeadDim];
 
     const int b = blockIdx.y;
     const int lane = threadIdx.x & 31;
@@ -87,13 +88,21 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         }
         mbar_init_fence();
     }
-    // Fold the group's query heads into Qp / Qn (q is an input of the step).
+    // Stage this request's query (Hq x 128 bf16, at most 16 KB) in shared
+    // memory with 16-byte loads, then fold each kv group's query heads into
+    // Qp / Qn.  q is an input of the step, so this overlaps the previous kernel.
     const int hq = HKV * group;
+    {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
+        uint4* qdst = reinterpret_cast<uint4*>(qstage);
+        for (int i = threadIdx.x; i < hq * kHeadDim / 8; i += kScoreThreads) qdst[i] = qsrc[i];
+    }
+    __syncthreads();
     for (int idx = threadIdx.x; idx < HKV * kHeadDim; idx += kScoreThreads) {
         const int j = idx / kHeadDim, ch = idx % kHeadDim;
         float qp = 0.f, qn = 0.f;
         for (int h = 0; h < group; ++h) {
-            const float v = __bfloat162float(q[(static_cast<int64_t>(b) * hq + j * group + h) * kHeadDim + ch]);
+            const float v = __bfloat162float(qstage[(j * group + h) * kHeadDim + ch]);
             qp += fmaxf(v, 0.f);
             qn += fminf(v, 0.f);
         }
@@ -262,7 +271,9 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide inclusive scan of one value per thread.
+// Block-wide inclusive scan of one value per thread.  With reuse = false the
+// caller promises not to touch warp_tot again, which saves a barrier.
+template <bool reuse = true>
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -283,7 +294,7 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
     }
     __syncthreads();
     const uint32_t add = warp > 0 ? warp_tot[warp - 1] : 0u;
-    __syncthreads();   // warp_tot may be reused right after
+    if (reuse) __syncthreads();   // warp_tot may be reused right after
     return v + add;
 }
 
@@ -328,8 +339,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     __shared__ uint32_t warp_lo[kTopkWarps], warp_hi[kTopkWarps];
     __shared__ uint32_t cand_key[kCandCap];
     __shared__ int32_t cand_idx[kCandCap];
-    __shared__ uint32_t s_bin, s_rem, s_cand, s_T, s_take, s_lo, s_shift;
-    __shared__ int32_t s_Tidx;
+    __shared__ uint32_t s_bin, s_rem, s_cand, s_T, s_take;
 
     const int bg = blockIdx.x;
     const int b = bg / num_kv_heads;
@@ -384,19 +394,12 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         warp_hi[warp] = hi;
     }
     __syncthreads();
-    if (warp == 0) {
-        lo = __reduce_min_sync(0xffffffffu, lane < kTopkWarps ? warp_lo[lane] : 0xffffffffu);
-        hi = __reduce_max_sync(0xffffffffu, lane < kTopkWarps ? warp_hi[lane] : 0u);
-        if (lane == 0) {
-            const uint32_t range = hi - lo;
-            const int bits = range == 0 ? 0 : 32 - __clz(range);   // range < 2^bits
-            s_lo = lo;
-            s_shift = bits > 11 ? bits - 11 : 0;                    // (range >> shift) < 2048
-        }
-    }
-    __syncthreads();
-    lo = s_lo;
-    const uint32_t shift = s_shift;
+    // Every warp folds the per-warp values itself (no second barrier).
+    lo = __reduce_min_sync(0xffffffffu, lane < kTopkWarps ? warp_lo[lane] : 0xffffffffu);
+    hi = __reduce_max_sync(0xffffffffu, lane < kTopkWarps ? warp_hi[lane] : 0u);
+    const uint32_t range = hi - lo;
+    const int range_bits = range == 0 ? 0 : 32 - __clz(range);            // range < 2^bits
+    const uint32_t shift = range_bits > 11 ? range_bits - 11 : 0;        // (range >> shift) < 2048
 
     // 2. histogram of (key - lo) >> shift; bin of the m-th best key.
 #pragma unroll
@@ -416,26 +419,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
                 cand_idx[pos] = i0 + e;
             }
         }
-        if (tid == 0) s_take = 0u;
         __syncthreads();
         const int nc = static_cast<int>(s_cand);
-        uint32_t my_k = 0;
-        int my_i = 0;
         if (tid < nc) {
-            my_k = cand_key[tid];
-            my_i = cand_idx[tid];
-            uint32_t rank = 0;
+            // rank = keys above mine + equal keys at lower pages; the candidate
+            // ranked need - 1 is the threshold T, and the keys equal to T that
+            // are taken are those ranked at or before it: need - (keys above T).
+            const uint32_t my_k = cand_key[tid];
+            const int my_i = cand_idx[tid];
+            uint32_t above = 0, tied_before = 0;
             for (int j = 0; j < nc; ++j) {
                 const uint32_t kj = cand_key[j];
-                rank += (kj > my_k) || (kj == my_k && cand_idx[j] < my_i);
+                above += kj > my_k;
+                tied_before += (kj == my_k && cand_idx[j] < my_i);
             }
-            if (rank == need - 1) {
+            if (above + tied_before == need - 1) {
                 s_T = my_k;
-                s_Tidx = my_i;
+                s_take = need - above;
             }
         }
-        __syncthreads();
-        if (tid < nc && my_k == s_T && my_i <= s_Tidx) atomicAdd(&s_take, 1u);
         __syncthreads();
         T = s_T;
         take = s_take;
@@ -475,7 +477,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     }
     const uint32_t gt = __popc(gt_mask), eq = __popc(eq_mask);
     const uint32_t packed = (gt << 16) | eq;   // n <= 32768 keeps both halves in 16 bits
-    const uint32_t excl = block_inclusive_scan(packed, warp_tot) - packed;
+    const uint32_t excl = block_inclusive_scan<false>(packed, warp_tot) - packed;
     const uint32_t eq_before = excl & 0xffffu;
     uint32_t sel_mask = gt_mask;
     uint32_t eq_take = take > eq_before ? min(take - eq_before, eq) : 0u;
