@@ -45,7 +45,8 @@ from query_aware_sparse_quest_gb300 import binding, build, resident, synth  # no
 METRIC = "sparse-decode steps/s and achieved HBM GB/s vs ~8 TB/s at 128k ctx, batch 8"
 UNIT = "steps/s"
 BENCH_CONFIG = 2
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "score_pages_qwen3_b8_ctx128000.txt")
+PROFILE_SUMMARIES = {"score_pages_kernel": "profiles/score_pages_qwen3_b8_ctx128000.txt",
+                     "flash_decode_split_kernel": "profiles/flash_decode_qwen3_b8_ctx128000.txt"}
 KERNEL_SOURCES = {"score_pages_kernel": "query_aware_sparse_quest_gb300/csrc/svq_select.cu",
                   "flash_decode_split_kernel": "query_aware_sparse_quest_gb300/csrc/svq_decode.cu"}
 
@@ -104,10 +105,11 @@ class ClockSampler:
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
-    if not os.path.exists(PROFILE_SUMMARY):
+    path = os.path.join(ROOT, PROFILE_SUMMARIES[kernel])
+    if not os.path.exists(path):
         return None
     vals = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             if "=" in line and not line.lstrip().startswith("#"):
                 k, v = line.split("=", 1)
@@ -143,6 +145,24 @@ def algorithmic_bytes(wl):
         "flash_decode_split_kernel": kv + sel_rd + q,
         "dense_step": dense_kv + pt + q + out,
     }
+
+
+def count_library_kernels(fn):
+    """Kernels of libsvquest.so that one call of `fn` launches, counted from
+    the CUDA activity trace of torch's profiler (None if unavailable)."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            fn()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        ours = [n for n in names if "svq::" in n or any(k in n for k in (
+            "score_pages_kernel", "topk_pages_kernel", "flash_decode_split_kernel", "lse_combine_kernel",
+            "append_kv_meta_kernel"))]
+        return len(ours) or None
+    except Exception:
+        return None
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -243,6 +263,7 @@ def run_gpu(args):
     for _ in range(3):
         step()
     torch.cuda.synchronize(dev)
+    launches_per_step = count_library_kernels(step)
     g_step = capture(step)
     g_dense = capture(dense)
     for _ in range(args.warmup):
@@ -343,7 +364,8 @@ def run_gpu(args):
                   "gbs": round(ab["dense_step"] / (dense_ms * 1e-3) / 1e9, 1), "bytes": ab["dense_step"]},
         "e2e": {"value": round(world * 1e3 / e2e_ms, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
-        "gpu_launches": 4 * args.steps,
+        "gpu_launches": None if launches_per_step is None else launches_per_step * args.steps,
+        "launches_per_step": launches_per_step,
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
