@@ -8,6 +8,7 @@
  *   on_kv_stored(...)      -> sv_quest_update_meta  (store K/V, refresh page metadata)
  *   build_decode_view(q)   -> sv_quest_select       (query-aware page selection)
  *   generic attention      -> sv_sparse_decode      (attention over the view)
+ * and sv_quest_decode_step runs the last two as one launch.
  *
  * Conventions common to every call
  *  - Every buffer argument is a DEVICE pointer, allocated and owned by the
@@ -182,6 +183,37 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
                                     int32_t max_pages, const int32_t* sel_idx, const int32_t* sel_cnt,
                                     int32_t budget_pages, float softmax_scale, void* out, float* lse,
                                     void* stream);
+
+/*
+ * sv_quest_decode_step -- one decode step in a single kernel launch:
+ * build_decode_view (page scores + top-K, as sv_quest_select) followed by
+ * attention over the view (as sv_sparse_decode): the decode-time hooks of
+ * the SparseEngine page ("method key points": query-relevant page selection
+ * before attention, then attention over the selected pages only) fused into
+ * one kernel.  The pages prescribe no kernel fusion; this is the same
+ * computation scheduled as one launch.  Results are those of
+ * sv_quest_select + sv_sparse_decode on the same inputs: sel_idx / sel_cnt
+ * identical up to page scores that differ only in fp32 rounding order, out /
+ * lse equal up to the split-K summation order.
+ *  - budget_pages >= 1 is the row length of sel_idx, as in sv_quest_select.
+ *  - softmax_scale > 0, as in sv_sparse_decode.
+ *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
+ *    with a call that may run at the same time; nothing in it needs to start
+ *    at zero (the call clears its own counters first).
+ *  - max_pages <= 8192 (131072 tokens) runs as one cooperative launch: every
+ *    CTA co-resident, so the call returns SV_ERR_CUDA if the device cannot
+ *    hold the grid (e.g. another context holds its SMs under MPS).  Larger
+ *    max_pages runs sv_quest_select then sv_sparse_decode inside the same
+ *    workspace.
+ */
+int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                         const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                         int32_t max_pages, int32_t budget_pages, float softmax_scale,
+                         int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t max_pages, int32_t budget_pages);
 
 /* Reads (and with reset != 0 clears) the current device's error word; the
  * read synchronises the device.  Returns SV_OK or SV_ERR_CUDA. */

@@ -53,6 +53,7 @@ def _load():
         "sv_quest_select": [cp, vp, i32, vp, vp, i32, i32, i32, vp, vp, vp, vp, sz, vp],
         "sv_sparse_decode": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp, sz, vp],
         "sv_sparse_decode_static_scratch": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp],
+        "sv_quest_decode_step": [cp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
         "sv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int],
     }
     for name, args in sig.items():
@@ -63,6 +64,8 @@ def _load():
     lib.sv_quest_select_workspace_size.restype = sz
     lib.sv_sparse_decode_workspace_size.argtypes = [i32, i32, i32, i32]
     lib.sv_sparse_decode_workspace_size.restype = sz
+    lib.sv_quest_decode_step_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+    lib.sv_quest_decode_step_workspace_size.restype = sz
     lib.sv_status_string.argtypes = [ctypes.c_int]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_version.argtypes = []
@@ -179,6 +182,24 @@ def sv_sparse_decode_static_scratch(cache: Cache, q: torch.Tensor, page_table: t
     _check("sv_sparse_decode_static_scratch", _load().sv_sparse_decode_static_scratch(
         cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
         _p(sel_cnt), K, scale, _p(out), _p(lse), _stream(stream)))
+
+
+def sv_quest_decode_step_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_pages: int,
+                                        budget_pages: int) -> int:
+    return int(_load().sv_quest_decode_step_workspace_size(batch, num_q_heads, num_kv_heads, max_pages,
+                                                           budget_pages))
+
+
+def sv_quest_decode_step(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                         budget_pages: int, sel_idx: torch.Tensor, sel_cnt: torch.Tensor, out: torch.Tensor,
+                         lse: torch.Tensor, workspace: torch.Tensor, softmax_scale: Optional[float] = None,
+                         stream=None) -> None:
+    B, Hq, D = q.shape
+    scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
+    _check("sv_quest_decode_step", _load().sv_quest_decode_step(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
+        scale, _p(sel_idx), _p(sel_cnt), _p(out), _p(lse), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def sv_get_device_error(reset: bool = True) -> int:

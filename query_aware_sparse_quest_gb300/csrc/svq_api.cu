@@ -22,8 +22,14 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
                   void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream);
 int decode_max_splits(int pages);
 size_t decode_workspace_bytes(int batch, int num_q_heads, int splits);
+int read_error_step(uint32_t* flags, int reset);
+int launch_step(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table, const int32_t* seq_lens,
+                int batch, int max_pages, int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, float softmax_scale,
+                void* out, float* lse, void* workspace, size_t ws_bytes, int sm_count, cudaStream_t stream);
+size_t step_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int max_pages, int budget_pages);
 
 constexpr int kMaxTopkPages = 32768;
+constexpr int kMaxStepPages = 8192;   // one top-K row per 256 threads x 32 keys in the fused step
 
 namespace {
 
@@ -167,12 +173,55 @@ int sv_sparse_decode(const sv_cache* cache, const void* q, int32_t num_q_heads, 
                          static_cast<cudaStream_t>(stream));
 }
 
+size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t max_pages, int32_t budget_pages) {
+    if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_pages < 1 || budget_pages < 1) return 0;
+    if (max_pages <= kMaxStepPages)
+        return step_workspace_bytes(batch, num_q_heads, num_kv_heads, max_pages, budget_pages);
+    return scores_bytes(batch, num_kv_heads, max_pages) +
+           decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
+}
+
+int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                         const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                         float softmax_scale, int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if (!sel_idx || !sel_cnt || !out || !lse || budget_pages < 1) return SV_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
+    if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * cache->num_kv_heads > 65535) return SV_ERR_UNSUPPORTED;
+    if (!workspace ||
+        workspace_bytes < sv_quest_decode_step_workspace_size(batch, num_q_heads, cache->num_kv_heads, max_pages,
+                                                              budget_pages))
+        return SV_ERR_WORKSPACE;
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (max_pages <= kMaxStepPages)
+        return launch_step(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, sel_idx,
+                           sel_cnt, softmax_scale, out, lse, workspace, workspace_bytes, sms, s);
+    // Two-stage path: scores at the front of the workspace, split-K partials after.
+    const size_t sb = scores_bytes(batch, cache->num_kv_heads, max_pages);
+    float* scores = static_cast<float*>(workspace);
+    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms, s))) return st;
+    if ((st = launch_topk(scores, seq_lens, batch, cache->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, s)))
+        return st;
+    return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
+                         budget_pages, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
+                         workspace_bytes - sb, sms, s);
+}
+
 int sv_get_device_error(uint32_t* flags, int reset) {
     if (!flags) return SV_ERR_INVALID_ARG;
     *flags = 0;
     int st;
     if ((st = read_error_meta(flags, reset))) return st;
     if ((st = read_error_select(flags, reset))) return st;
+    if ((st = read_error_step(flags, reset))) return st;
     return read_error_decode(flags, reset);
 }
 

@@ -127,3 +127,41 @@ def test_update_meta_rejects_bad_args(lib):
     assert lib.sv_quest_update_meta(c, None, FAKE, FAKE, 4, None) == SV_ERR_INVALID_ARG
     bad = ctypes.byref(_fake_cache(page_size=8))
     assert lib.sv_quest_update_meta(bad, FAKE, FAKE, FAKE, 4, None) == SV_ERR_UNSUPPORTED
+
+
+def test_decode_step_workspace_size(lib):
+    f = binding.sv_quest_decode_step_workspace_size
+    # fused path: scores + split-K partials (16 pages per split, <= 64 splits) + counters
+    ws = f(8, 32, 4, 8000, 256)
+    assert ws >= 8 * 4 * 8000 * 4 + 8 * 32 * 16 * (128 * 4 + 8) + (1 + 8 + 2 * 32) * 4
+    assert f(8, 32, 4, 8000, 256) < f(8, 32, 4, 8000, 512)
+    # two-stage path above 8192 pages: select scores + sparse-decode partials
+    assert f(2, 8, 1, 9000, 64) >= (binding.sv_quest_select_workspace_size(2, 1, 9000)
+                                    + binding.sv_sparse_decode_workspace_size(2, 8, 1, 64))
+    assert f(0, 32, 4, 100, 16) == 0
+    assert f(8, 32, 4, 100, 0) == 0
+
+
+def test_decode_step_rejects_bad_args(lib):
+    c = ctypes.byref(_fake_cache())
+
+    def call(q=FAKE, hq=32, batch=8, max_pages=100, K=16, scale=0.088, sel=FAKE, cnt=FAKE, out=FAKE,
+             lse=FAKE, ws=FAKE, ws_bytes=1 << 30, cache=c):
+        return lib.sv_quest_decode_step(cache, q, hq, FAKE, FAKE, batch, max_pages, K, scale, sel, cnt, out, lse,
+                                        ws, ws_bytes, None)
+    assert call(q=None) == SV_ERR_INVALID_ARG
+    assert call(sel=None) == SV_ERR_INVALID_ARG
+    assert call(cnt=None) == SV_ERR_INVALID_ARG
+    assert call(out=None) == SV_ERR_INVALID_ARG
+    assert call(lse=None) == SV_ERR_INVALID_ARG
+    assert call(K=0) == SV_ERR_INVALID_ARG
+    assert call(batch=0) == SV_ERR_INVALID_ARG
+    assert call(scale=0.0) == SV_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == SV_ERR_INVALID_ARG
+    assert call(hq=30) == SV_ERR_INVALID_ARG
+    assert call(max_pages=40000) == SV_ERR_UNSUPPORTED
+    assert call(cache=ctypes.byref(_fake_cache(page_size=32))) == SV_ERR_UNSUPPORTED
+    assert call(ws=None) == SV_ERR_WORKSPACE
+    need = binding.sv_quest_decode_step_workspace_size(8, 32, 4, 100, 16)
+    assert call(ws_bytes=need - 1) == SV_ERR_WORKSPACE
+    assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
