@@ -3,24 +3,29 @@
 // combine -- as one persistent, cooperative launch (two CTAs per SM, all
 // co-resident).
 //
-// Work split:
-//   scoring   : CTAs 0 .. score_ctas-1 stream, for request 0, 1, ..., B-1 in
-//               turn, their slice of the request's page metadata (TMA bulk copies
-//               into a shared-memory ring; producer warp + eight consumer warps)
-//               and write the page scores, with no drain between requests.
-//   queue     : request-major items -- per request, one top-K selection item
-//               per kv head, then (kv head, split) attention items.  The other
-//               CTAs take items from the start; score CTAs join when their
-//               scoring is done.  A selection item waits until every score CTA
-//               has finished the request; an attention item waits for its kv
-//               head's selection, streams the split's K/V boxes by TMA and runs
-//               the tensor-core flash-decode loop; the CTA that finishes the
-//               last split of a (request, kv head) combines the splits by
-//               log-sum-exp.
-// So request b's selection and attention overlap the scoring of requests
-// b+1, ..., and HBM stays busy through the latency-bound top-K.  Every
-// cross-CTA wait is bounded and is on work owned by a co-resident CTA that
-// does not wait on the waiter.
+// Every CTA has eight compute warps, a producer warp (TMA) and a control warp
+// that does all of the CTA's cross-CTA signalling (work claims, readiness
+// waits, releases), so compute warps never stall on a global round trip.
+// Roles, by CTA index:
+//   score     : stream, request by request, this CTA's slice of the page
+//               metadata (bulk copies into a shared-memory ring) and write the
+//               page scores; the control warp publishes "slice of request b
+//               scored" once all eight compute warps are past it.
+//   selector  : per (request, kv head) of its share, wait until every score
+//               CTA has published the request, run the top-K over the score row
+//               and publish the selection.
+//   then all  : a request-major queue of attention items -- (request, kv head,
+//               split) page ranges of the selection, then one combine item per
+//               (request, kv head), placed one request later.  The control warp
+//               claims an item and waits for its inputs, the producer streams
+//               the split's K/V boxes while the compute warps still work on the
+//               previous item, and the compute warps run the tensor-core flash
+//               decode loop; a combine item merges the splits by log-sum-exp.
+// So the selection and attention of request b overlap the scoring of b+1, ...
+// Every cross-CTA wait is bounded and waits on work that a co-resident CTA
+// owns and finishes without waiting on the waiter: score CTAs wait on nothing,
+// selectors on score CTAs, attention items on selectors, combine items on
+// attention items of lower queue index.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -31,27 +36,45 @@ namespace svq {
 
 SVQ_DEFINE_ERROR_WORD(read_error_step)
 
-constexpr int kStepConsumers = 8;
-constexpr int kStepThreads = (kStepConsumers + 1) * 32;
-constexpr int kStepProducer = kStepConsumers;
+constexpr int kStepConsumers = 8;                          // compute warps
+constexpr int kStepProducer = kStepConsumers;              // warp 8
+constexpr int kStepControl = kStepConsumers + 1;           // warp 9
+constexpr int kStepThreads = (kStepConsumers + 2) * 32;    // 320
+constexpr int kComputeThreads = kStepConsumers * 32;       // 256
 constexpr int kStepRingBytes = 64 * 1024;
-constexpr int kStepSmem = kStepRingBytes + 1024;          // + slack for 1024-byte alignment
-constexpr int kBox = kPage * 64 * 2;                      // 16 x 64 bf16 TMA box (2 KB)
-constexpr int kKvStage = 4 * kBox;                        // K lo | K hi | V lo | V hi
-constexpr int kKvStages = kStepRingBytes / kKvStage;      // 8: stage s is consumed by warp s
-constexpr int kTopkThreadsStep = kStepConsumers * 32;     // 256
-constexpr int kTopkItemsStep = 32;                        // rows up to 8192 pages
+constexpr int kBox = kPage * 64 * 2;                       // 16 x 64 bf16 TMA box (2 KB)
+constexpr int kKvStage = 4 * kBox;                         // K lo | K hi | V lo | V hi
+constexpr int kKvStages = kStepRingBytes / kKvStage;       // 8: stage s is consumed by warp s
+constexpr int kTopkItems = 32;                             // keys per thread
+constexpr int kStepMaxPages = kComputeThreads * kTopkItems;  // 8192 pages (131072 tokens) per request
 constexpr int kStepBins = 2048;
 constexpr int kStepCandCap = 256;
-constexpr uint32_t kSpinLimit = 1u << 24;                 // polls of a cross-CTA counter before giving up
 constexpr int kStepMaxSplits = 64;
-constexpr int kStepMaxPages = kTopkThreadsStep * kTopkItemsStep;   // 8192 pages (131072 tokens) per request
-static_assert(kKvStages == kStepConsumers, "each ring stage belongs to one consumer warp");
+constexpr uint32_t kSpinLimit = 1u << 24;                  // polls of a cross-CTA counter before giving up
+// Merge area for the eight warps' partial outputs: o [8][8 heads][128] + m, l [8][8].
+constexpr int kMergeBytes = kStepConsumers * kMaxGroup * (kHeadDim + 2) * 4;
+static_assert(kKvStages == kStepConsumers, "each ring stage belongs to one compute warp");
+static_assert(kStepMaxPages * 4 <= kStepRingBytes, "a score row must fit the ring for the top-K");
+
+#ifndef SVQ_STEP_PAGES_PER_SPLIT
+#define SVQ_STEP_PAGES_PER_SPLIT 16
+#endif
+#ifndef SVQ_STEP_SCORE_PERMILLE
+#define SVQ_STEP_SCORE_PERMILLE 0   // 0: one score CTA per SM
+#endif
+#ifndef SVQ_STEP_SELECTORS_PER_HEAD
+#define SVQ_STEP_SELECTORS_PER_HEAD 4
+#endif
+#ifndef SVQ_STEP_POLL_NS
+#define SVQ_STEP_POLL_NS 256   // sleep between polls of a cross-CTA counter
+#endif
+#ifndef SVQ_STEP_IDLE_NS
+#define SVQ_STEP_IDLE_NS 128   // sleep between polls of an idle warp waiting for its next item
+#endif
 
 struct StepArgs {
     const __nv_bfloat16* meta;
     int64_t num_phys_pages;
-    int num_kv_heads;
     const __nv_bfloat16* q;
     int num_q_heads;
     int group;
@@ -61,40 +84,82 @@ struct StepArgs {
     int max_pages;
     int K;
     float scale_log2;
-    float* scores;            // [B][Hkv][max_pages]
+    float* scores;            // [B][Hkv][score_stride]
+    int score_stride;         // max_pages rounded up to 32
     int32_t* sel_idx;         // [B][Hkv][K]
     int32_t* sel_cnt;         // [B][Hkv]
     float* o_part;            // [B][Hq][splits][128]
     float2* ml_part;          // [B][Hq][splits]
     __nv_bfloat16* out;       // [B][Hq][128]
     float* lse;               // [B][Hq]
-    int score_ctas;           // CTAs 0 .. score_ctas-1 score; the rest decode
-    int splits;               // decode items per (request, kv head)
-    uint32_t* ctr;            // [0] next decode item, [1 + b] score slices done,
-                              // [1 + B + bg] selection ready, [1 + B + BH + bg] splits done
+    int score_ctas;           // CTAs [0, score_ctas) score
+    int sel_ctas;             // CTAs [score_ctas, score_ctas + sel_ctas) select
+    int splits;               // attention items per (request, kv head)
+    uint32_t* ctr;            // [0] next queue item, [1 + b] score CTAs done with request b,
+                              // [1 + B + bg] selection of bg published, [1 + B + BH + bg] splits done
 };
 
+// ---------------------------------------------------------------- small helpers
 __device__ __forceinline__ float step_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// Order-preserving map of a float to u32 (larger float -> larger key).
 __device__ __forceinline__ uint32_t step_order_key(float f) {
     const uint32_t u = __float_as_uint(f);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+// 128-byte swizzle of a 16 x 64 bf16 box (chunk = 16 bytes).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
-__device__ __forceinline__ void consumers_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kTopkThreadsStep) : "memory"); }
+// Barrier of the eight compute warps only.
+__device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kComputeThreads) : "memory"); }
 
-// Polls a counter written by other CTAs until it reaches `target` (bounded).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Data that other CTAs of this launch wrote is read after an acquire (by this
+// thread, or by another thread followed by a barrier) with L2 loads (__ldcg),
+// which the compiler may batch; L1 may hold stale copies, L2 does not.
+__device__ __forceinline__ int ld_relaxed_i32(const int32_t* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Adds v to a global counter, ordered after every write this thread has
+// observed (its own and, through barriers, its CTA's).
+__device__ __forceinline__ void red_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_release_cta_smem(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta_smem(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(p)) : "memory");
+    return v;
+}
+
+// Polls a counter written by other CTAs until it reaches `target` (acquire;
+// bounded).
 __device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target) {
     for (uint32_t it = 0; it < kSpinLimit; ++it) {
-        uint32_t v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-        if (v >= target) return true;
-        __nanosleep(64);
+        if (ld_acquire_gpu(p) >= target) return true;
+        __nanosleep(SVQ_STEP_POLL_NS);
+    }
+    return false;
+}
+
+// Waits for an item-slot phase; the waiting warps sleep between polls so
+// that they take few issue slots from the CTA that shares their SM.
+__device__ __forceinline__ bool wait_item(uint32_t bar, uint32_t parity) {
+    for (uint32_t it = 0; it < kMbarPollLimit; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (SVQ_STEP_IDLE_NS > 0) __nanosleep(SVQ_STEP_IDLE_NS);
     }
     return false;
 }
@@ -114,69 +179,149 @@ struct StepScoreShape {
     static constexpr int kPageBytes = HKV * 2 * kHeadDim * 2;          // one page's metadata, all kv heads
     static constexpr int kSlots = kStepRingBytes / kPageBytes;          // 128 / 64 / 32 / 16 for HKV 1 / 2 / 4 / 8
     static constexpr int R = kSlots < 32 ? kSlots : 32;                 // pages issued per producer round
-    static constexpr int L = 32 / HKV;                                  // consumer lanes per kv head
+    static constexpr int L = 32 / HKV;                                  // compute lanes per kv head
     static constexpr int C = HKV;                                       // 16-byte chunks per lane per page
     static constexpr int kQBufBytes = kMaxGroup * HKV * kHeadDim * 2;   // one request's queries, at most
     static_assert(kSlots % R == 0 && kSlots % kStepConsumers == 0, "score ring shape");
+    static_assert(2 * kQBufBytes <= kMergeBytes, "query buffers live in the merge area");
 };
 
-// ---------------------------------------------------------------- top-K (256 consumer threads)
-// Same selection as topk_pages_kernel: keys in registers (32 consecutive pages
-// per thread), min/max-adaptive histogram, exact rank among the boundary
-// bin's keys (radix fallback), ordered compaction from bit masks.
+// ---------------------------------------------------------------- queue items
+// Request-major: F(0), F(1), C(0), F(2), C(1), ..., F(B-1), C(B-2), C(B-1),
+// where F(b) = Hkv * splits attention items and C(b) = Hkv combine items.
+struct QueueItem {
+    int kind;   // 0 stop, 1 attention, 2 combine
+    int b, g, split;
+};
+template <int HKV>
+__device__ __forceinline__ QueueItem decode_item(const StepArgs& a, int item) {
+    QueueItem it{0, 0, 0, 0};
+    const int nf = HKV * a.splits;
+    const int total = a.batch * (nf + HKV);
+    if (item < 0 || item >= total) return it;
+    int j, r;
+    if (item < nf) {
+        j = 0;
+        r = item;
+    } else {
+        const int x = item - nf;
+        j = 1 + x / (nf + HKV);
+        r = x - (j - 1) * (nf + HKV);
+    }
+    if (j < a.batch && r < nf) {
+        it.kind = 1;
+        it.b = j;
+        it.g = r / a.splits;
+        it.split = r - it.g * a.splits;
+    } else {
+        it.kind = 2;
+        it.b = j - 1;
+        it.g = j < a.batch ? r - nf : r;
+    }
+    return it;
+}
+
+// ---------------------------------------------------------------- top-K of one score row (256 compute threads)
+// Keeps the m = min(K, n) highest scores (ties to the lower page index) and
+// writes their indices in ascending order.  The row is staged through shared
+// memory with coalesced loads; thread t then holds keys 32t .. 32t+31.  A
+// lower bound on the m-th largest key (the smallest j-th largest key over
+// threads, for the smallest j in 1..4 with enough keys at or above it) trims
+// the adaptive histogram to the top of the row; the boundary bin's keys are
+// ranked exactly (radix passes when the bin holds more than 256 keys); the
+// compaction follows the index order.
 struct TopkScratch {
     uint32_t hist[kStepBins];
     uint32_t warp_tot[kStepConsumers];
-    uint32_t warp_lo[kStepConsumers], warp_hi[kStepConsumers];
+    uint32_t warp_red[6][kStepConsumers];
     uint32_t cand_key[kStepCandCap];
     int32_t cand_idx[kStepCandCap];
     uint32_t bin, rem, cand, T, take;
 };
 
-__device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
+__device__ void select_row(const StepArgs& a, TopkScratch& sc, float* stage, int bg, int n) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = a.K;
     const int m = min(K, n);
     int32_t* out = a.sel_idx + static_cast<int64_t>(bg) * K;
     if (n <= K) {
-        for (int i = tid; i < K; i += kTopkThreadsStep) out[i] = i < n ? i : -1;
-        if (tid == 0) a.sel_cnt[bg] = n;
+        for (int i = tid; i < K; i += kComputeThreads) out[i] = i < n ? i : -1;
+        if (tid == 0) a.sel_cnt[bg] = n < 0 ? 0 : n;
         return;
     }
-    const float* row = a.scores + static_cast<int64_t>(bg) * a.max_pages;
-    const int i0 = kTopkItemsStep * tid;
-    uint32_t key[kTopkItemsStep];
-    uint32_t lo = 0xffffffffu, hi = 0u;
+    // Coalesced 16-byte loads -> swizzled shared memory -> 32 consecutive keys per thread.
+    const float* row = a.scores + static_cast<int64_t>(bg) * a.score_stride;
 #pragma unroll
-    for (int e = 0; e < kTopkItemsStep; ++e) {
-        float f;
-        asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(f) : "l"(row + min(i0 + e, a.max_pages - 1)) : "memory");
-        key[e] = step_order_key(f);
-        if (i0 + e < n) {
-            lo = min(lo, key[e]);
-            hi = max(hi, key[e]);
-        }
+    for (int e = 0; e < kTopkItems / 4; ++e) {
+        const int idx = 4 * tid + 4 * kComputeThreads * e;
+        const float4 v = idx < a.score_stride ? __ldcg(reinterpret_cast<const float4*>(row + idx))
+                                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        const int owner = (tid >> 3) + (kComputeThreads / 8) * e;
+        const int chunk = tid & 7;
+        *reinterpret_cast<float4*>(stage + owner * 32 + 4 * (chunk ^ (owner & 7))) = v;
     }
-    for (int i = tid; i < kStepBins; i += kTopkThreadsStep) sc.hist[i] = 0u;
-    if (tid == 0) sc.cand = 0u;
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    if (lane == 0) {
-        sc.warp_lo[warp] = lo;
-        sc.warp_hi[warp] = hi;
+    compute_sync();
+    const int i0 = kTopkItems * tid;
+    uint32_t key[kTopkItems];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float4 v = *reinterpret_cast<const float4*>(stage + tid * 32 + 4 * (c ^ (tid & 7)));
+        key[4 * c] = step_order_key(v.x);
+        key[4 * c + 1] = step_order_key(v.y);
+        key[4 * c + 2] = step_order_key(v.z);
+        key[4 * c + 3] = step_order_key(v.w);
     }
-    consumers_sync();
-    lo = __reduce_min_sync(0xffffffffu, lane < kStepConsumers ? sc.warp_lo[lane] : 0xffffffffu);
-    hi = __reduce_max_sync(0xffffffffu, lane < kStepConsumers ? sc.warp_hi[lane] : 0u);
+    // Row minimum / maximum and, per thread, the maxima of its four groups of
+    // 8 keys sorted (q1 >= q2 >= q3 >= q4): the thread holds at least j keys
+    // >= qj, one from each of j groups.
+    uint32_t kmin = 0xffffffffu, kmax = 0u;
+    uint32_t qmax[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int e = 0; e < kTopkItems; ++e) {
+        const bool v = i0 + e < n;
+        kmin = min(kmin, v ? key[e] : 0xffffffffu);
+        qmax[e >> 3] = max(qmax[e >> 3], v ? key[e] : 0u);
+    }
+    kmax = max(max(qmax[0], qmax[1]), max(qmax[2], qmax[3]));
+    {
+        uint32_t x;
+#define SVQ_CSWAP(i, j) x = min(qmax[i], qmax[j]); qmax[i] = max(qmax[i], qmax[j]); qmax[j] = x;
+        SVQ_CSWAP(0, 1) SVQ_CSWAP(2, 3) SVQ_CSWAP(0, 2) SVQ_CSWAP(1, 3) SVQ_CSWAP(1, 2)
+#undef SVQ_CSWAP
+    }
+    const bool full = i0 + kTopkItems <= n;   // only threads with 32 valid keys give bounds
+    uint32_t red[6] = {kmin, kmax, full ? qmax[0] : 0xffffffffu, full ? qmax[1] : 0xffffffffu,
+                       full ? qmax[2] : 0xffffffffu, full ? qmax[3] : 0xffffffffu};
+    for (int i = tid; i < kStepBins; i += kComputeThreads) sc.hist[i] = 0u;
+#pragma unroll
+    for (int r = 0; r < 6; ++r) {
+        const uint32_t v = r == 1 ? __reduce_max_sync(0xffffffffu, red[r]) : __reduce_min_sync(0xffffffffu, red[r]);
+        if (lane == 0) sc.warp_red[r][warp] = v;
+    }
+    compute_sync();
+#pragma unroll
+    for (int r = 0; r < 6; ++r) {
+        const uint32_t v = lane < kStepConsumers ? sc.warp_red[r][lane] : (r == 1 ? 0u : 0xffffffffu);
+        red[r] = r == 1 ? __reduce_max_sync(0xffffffffu, v) : __reduce_min_sync(0xffffffffu, v);
+    }
+    // Lower bound on the m-th largest key: the full threads each hold j keys
+    // >= the minimum over them of qj, so that minimum is a bound once
+    // j * (number of full threads) >= m; the smallest such j gives the tightest.
+    uint32_t lo = red[0];
+    const int full_threads = min(kComputeThreads, n / kTopkItems);
+#pragma unroll
+    for (int j = 4; j >= 1; --j)
+        if (j * full_threads >= m) lo = red[1 + j];
+    const uint32_t hi = red[1];
     const uint32_t range = hi - lo;
     const int rbits = range == 0 ? 0 : 32 - __clz(range);
     const uint32_t shift = rbits > 11 ? rbits - 11 : 0;
 #pragma unroll
-    for (int e = 0; e < kTopkItemsStep; ++e)
-        if (i0 + e < n) atomicAdd(&sc.hist[(key[e] - lo) >> shift], 1u);
-    consumers_sync();
+    for (int e = 0; e < kTopkItems; ++e)
+        if (i0 + e < n && key[e] >= lo) atomicAdd(&sc.hist[(key[e] - lo) >> shift], 1u);
+    compute_sync();
     auto find_bin = [&](uint32_t remaining) {
-        constexpr int kBpt = kStepBins / kTopkThreadsStep;
+        constexpr int kBpt = kStepBins / kComputeThreads;
         const uint32_t top = kStepBins - 1 - kBpt * tid;
         uint32_t cnt[kBpt];
         uint32_t sum = 0;
@@ -188,11 +333,11 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
         uint32_t v = sum;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t2 = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += t2;
+            const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += t;
         }
         if (lane == 31) sc.warp_tot[warp] = v;
-        consumers_sync();
+        compute_sync();
         uint32_t add = 0;
         for (int w2 = 0; w2 < warp; ++w2) add += sc.warp_tot[w2];
         uint32_t before = v + add - sum;
@@ -204,21 +349,44 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
             }
             before += cnt[i];
         }
-        consumers_sync();
+        compute_sync();
     };
     find_bin(static_cast<uint32_t>(m));
     const uint32_t bstar = sc.bin, need = sc.rem;
     uint32_t T, take;
     if (sc.hist[bstar] <= kStepCandCap) {
+        // Keys of the boundary bin: per-thread mask, positions by a block scan.
+        uint32_t cmask = 0;
 #pragma unroll
-        for (int e = 0; e < kTopkItemsStep; ++e) {
-            if (i0 + e < n && ((key[e] - lo) >> shift) == bstar) {
-                const uint32_t pos = atomicAdd(&sc.cand, 1u);
+        for (int e = 0; e < kTopkItems; ++e)
+            cmask |= ((i0 + e < n && key[e] >= lo && ((key[e] - lo) >> shift) == bstar) ? 1u : 0u) << e;
+        const uint32_t cnt = __popc(cmask);
+        uint32_t incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        if (lane == 31) sc.warp_tot[warp] = incl;
+        compute_sync();
+        uint32_t pos = incl - cnt;
+        uint32_t total = 0;
+#pragma unroll
+        for (int w2 = 0; w2 < kStepConsumers; ++w2) {
+            const uint32_t t = sc.warp_tot[w2];
+            pos += w2 < warp ? t : 0u;
+            total += t;
+        }
+#pragma unroll
+        for (int e = 0; e < kTopkItems; ++e) {   // static indices keep key[] in registers
+            if ((cmask >> e) & 1u) {
                 sc.cand_key[pos] = key[e];
                 sc.cand_idx[pos] = i0 + e;
+                ++pos;
             }
         }
-        consumers_sync();
+        if (tid == 0) sc.cand = total;
+        compute_sync();
         const int nc = static_cast<int>(sc.cand);
         if (tid < nc) {
             const uint32_t my_k = sc.cand_key[tid];
@@ -234,24 +402,24 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
                 sc.take = need - above;
             }
         }
-        consumers_sync();
+        compute_sync();
         T = sc.T;
         take = sc.take;
     } else {
+        // Radix select on the full keys: 11 + 11 + 10 bits.
         uint32_t prefix = 0, remaining = static_cast<uint32_t>(m);
-        const int kSh[3] = {21, 10, 0};
-        const int kBi[3] = {11, 11, 10};
         for (int pass = 0; pass < 3; ++pass) {
-            const int sh = kSh[pass];
-            const uint32_t nbins = 1u << kBi[pass];
-            const uint32_t hi_mask = (pass == 0) ? 0u : ~((1u << (sh + kBi[pass])) - 1u);
-            consumers_sync();
-            for (int i = tid; i < kStepBins; i += kTopkThreadsStep) sc.hist[i] = 0u;
-            consumers_sync();
+            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+            const int nbits = pass == 2 ? 10 : 11;
+            const uint32_t nbins = 1u << nbits;
+            const uint32_t hi_mask = pass == 0 ? 0u : ~((1u << (sh + nbits)) - 1u);
+            compute_sync();
+            for (int i = tid; i < kStepBins; i += kComputeThreads) sc.hist[i] = 0u;
+            compute_sync();
 #pragma unroll
-            for (int e = 0; e < kTopkItemsStep; ++e)
+            for (int e = 0; e < kTopkItems; ++e)
                 if (i0 + e < n && (key[e] & hi_mask) == prefix) atomicAdd(&sc.hist[(key[e] >> sh) & (nbins - 1u)], 1u);
-            consumers_sync();
+            compute_sync();
             find_bin(remaining);
             prefix |= sc.bin << sh;
             remaining = sc.rem;
@@ -261,7 +429,7 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
     }
     uint32_t gt_mask = 0, eq_mask = 0;
 #pragma unroll
-    for (int e = 0; e < kTopkItemsStep; ++e) {
+    for (int e = 0; e < kTopkItems; ++e) {
         if (i0 + e < n) {
             gt_mask |= (key[e] > T ? 1u : 0u) << e;
             eq_mask |= (key[e] == T ? 1u : 0u) << e;
@@ -271,12 +439,11 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
     uint32_t v = packed;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t2 = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t2;
+        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += t;
     }
-    consumers_sync();   // everyone has read warp_tot of the last find_bin
     if (lane == 31) sc.warp_tot[warp] = v;
-    consumers_sync();
+    compute_sync();
     uint32_t add = 0;
     for (int w2 = 0; w2 < warp; ++w2) add += sc.warp_tot[w2];
     const uint32_t excl = v + add - packed;
@@ -296,81 +463,124 @@ __device__ void step_topk(const StepArgs& a, TopkScratch& sc, int bg, int n) {
         if (pos < static_cast<uint32_t>(m)) out[pos] = i0 + e;
         ++pos;
     }
-    for (int i = m + tid; i < K; i += kTopkThreadsStep) out[i] = -1;
+    for (int i = m + tid; i < K; i += kComputeThreads) out[i] = -1;
     if (tid == 0) a.sel_cnt[bg] = m;
 }
 
 // ---------------------------------------------------------------- score role
-// Streams this CTA's slice of every request's page metadata through the ring
-// (slot = sequence % slots; consumer warp = sequence % 8, so each slot has
-// one waiting warp) and writes the page scores.  The producer issues the pages
-// of one round from different lanes, each lane on its own slot.
+// Producer: streams this CTA's slices of all requests as one flat sequence of
+// pages, request-major, into ring slots (slot = sequence % slots), one page per
+// lane per round; the page-table entries of the next round are loaded while
+// the current round waits for free slots.  Compute warp w takes sequence
+// numbers = w (mod 8), so each slot has one waiting warp.  Control warp:
+// copies request b + 2's queries into q buffer b % 2 once the compute warps
+// have folded request b's, and publishes request b once all eight compute
+// warps are past it.
 template <int HKV>
 __device__ __forceinline__ void score_role(const StepArgs& a, unsigned char* ring, uint32_t ring_s, uint32_t full0,
                                            uint32_t empty0, unsigned char* slot_ok, const __nv_bfloat16* qbuf,
-                                           uint32_t qbuf_s, uint32_t qfull0, uint32_t qempty0, uint32_t* ctr_sdone) {
+                                           uint32_t qbuf_s, uint32_t qfull0, uint32_t qempty0, uint32_t* req_done) {
     using SS = StepScoreShape<HKV>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
-    const uint32_t q_bytes = static_cast<uint32_t>(a.num_q_heads) * kHeadDim * 2;
-    if (warp == kStepProducer) {
-        const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(a.meta);
-        const unsigned char* q_src = reinterpret_cast<const unsigned char*>(a.q);
-        uint32_t seq = 0;
-        bool failed = false;
-        for (int b = 0; b < a.batch && !failed; ++b) {
-            // Request b's queries (num_q_heads x 128 bf16, contiguous) into q
-            // buffer b % 2, once the consumers have folded request b - 2's.
-            if (lane == 0) {
+    if (warp == kStepControl) {
+        if (lane == 0) {
+            const uint32_t q_bytes = static_cast<uint32_t>(a.num_q_heads) * kHeadDim * 2;
+            const unsigned char* q_src = reinterpret_cast<const unsigned char*>(a.q);
+            auto stage_q = [&](int b) {
                 const int qb = b & 1;
-                const uint32_t use = static_cast<uint32_t>(b) >> 1;
-                bool okq = true;
-                if (use >= 1) okq = mbar_wait_bounded(qempty0 + qb * 8, (use - 1) & 1);
-                if (okq) {
-                    mbar_arrive_expect_tx(qfull0 + qb * 8, q_bytes);
-                    bulk_copy_g2s(qbuf_s + qb * SS::kQBufBytes, q_src + static_cast<int64_t>(b) * q_bytes, q_bytes,
-                                  qfull0 + qb * 8);
-                } else {
-                    failed = true;
+                mbar_arrive_expect_tx(qfull0 + qb * 8, q_bytes);
+                bulk_copy_g2s(qbuf_s + qb * SS::kQBufBytes, q_src + static_cast<int64_t>(b) * q_bytes, q_bytes,
+                              qfull0 + qb * 8);
+            };
+            stage_q(0);
+            if (a.batch > 1) stage_q(1);
+            uint32_t* sdone = a.ctr + 1;
+            for (int b = 0; b < a.batch; ++b) {
+                if (b + 2 < a.batch) {
+                    if (mbar_wait_bounded(qempty0 + (b & 1) * 8, (static_cast<uint32_t>(b) >> 1) & 1))
+                        stage_q(b + 2);
+                    else
+                        svq_flag(SV_DEVERR_TIMEOUT);
                 }
-            }
-            failed = __shfl_sync(0xffffffffu, failed, 0);
-            if (failed) break;
-            int len;
-            const int n = pages_of(a, b, len);
-            const int spp = (n + a.score_ctas - 1) / a.score_ctas;
-            const int lo = min(n, c * spp), hi = min(n, lo + spp);
-            const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
-            for (int base = lo; base < hi; base += SS::R) {
-                const int p = base + lane;
-                bool ok = true;
-                if (lane < SS::R && p < hi) {
-                    const uint32_t sq = seq + (p - lo);
-                    const int slot = sq % SS::kSlots;
-                    if (sq >= SS::kSlots) ok = mbar_wait_bounded(empty0 + slot * 8, ((sq / SS::kSlots) - 1) & 1);
-                    if (ok) {
-                        const int phys = pt_row[p];
-                        const uint32_t fb = full0 + slot * 8;
-                        const bool real = phys >= 0 && phys < a.num_phys_pages;
-                        slot_ok[slot] = real ? 1 : 0;
-                        if (real) {
-                            mbar_arrive_expect_tx(fb, SS::kPageBytes);
-                            bulk_copy_g2s(ring_s + slot * SS::kPageBytes,
-                                          meta_bytes + static_cast<int64_t>(phys) * SS::kPageBytes, SS::kPageBytes, fb);
-                        } else {
-                            svq_flag(SV_DEVERR_PAGE_TABLE);
-                            mbar_arrive(fb);
-                        }
+                bool ok = false;
+                for (uint32_t it = 0; it < kSpinLimit; ++it) {
+                    if (ld_acquire_cta_smem(req_done) >= static_cast<uint32_t>(kStepConsumers) * (b + 1)) {
+                        ok = true;
+                        break;
                     }
+                    __nanosleep(32);
                 }
-                if (__any_sync(0xffffffffu, !ok)) {
-                    failed = true;
-                    break;
+                if (!ok) svq_flag(SV_DEVERR_TIMEOUT);
+                red_release_gpu(sdone + b, 1u);
+            }
+        }
+        return;
+    }
+    if (warp == kStepProducer) {
+        // Lane l streams the pages at flat positions l, l + R, l + 2R, ... on its
+        // own (no warp-wide rounds), so each slot is refilled as soon as its
+        // page is consumed; the page-table entry of the lane's next page is
+        // loaded before it waits for the current slot.
+        if (lane >= SS::R) return;
+        const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(a.meta);
+        const int B = a.batch;
+        // Slice [lo, hi) of request b (clamped like pages_of, which flags).
+        auto slice = [&](int b, int& lo, int& hi) {
+            const int len = __ldg(a.seq_lens + b);
+            const int n = len < 1 ? 0 : min(a.max_pages, (len + kPage - 1) / kPage);
+            const int spp = (n + a.score_ctas - 1) / a.score_ctas;
+            lo = min(n, c * spp);
+            hi = min(n, lo + spp);
+        };
+        // Moves cursor (b, p) t pages forward in the flat sequence; b = B past the end.
+        auto advance = [&](int& b, int& p, int t) {
+            int lo = 0, hi = 0;
+            if (b < B) slice(b, lo, hi);
+            while (b < B && p + t >= hi) {
+                t -= hi - p;
+                if (++b < B) {
+                    slice(b, lo, hi);
+                    p = lo;
                 }
             }
-            seq += hi - lo;
+            p += t;
+        };
+        auto fetch = [&](int b, int p) -> int {
+            return b < B ? __ldg(a.page_table + static_cast<int64_t>(b) * a.max_pages + p) : -1;
+        };
+        int cb = 0, cp;
+        {
+            int lo, hi;
+            slice(0, lo, hi);
+            cp = lo;
         }
-        if (failed && lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
+        advance(cb, cp, lane);
+        int phys = fetch(cb, cp);
+        bool ok = true;
+        for (uint32_t f = lane; cb < B; f += SS::R) {
+            int nb = cb, np = cp;
+            advance(nb, np, SS::R);
+            const int phys_next = fetch(nb, np);
+            const int slot = f % SS::kSlots;
+            if (f >= SS::kSlots) ok = mbar_wait_bounded(empty0 + slot * 8, ((f / SS::kSlots) - 1) & 1);
+            if (!ok) break;
+            const uint32_t fb = full0 + slot * 8;
+            const bool real = phys >= 0 && phys < a.num_phys_pages;
+            slot_ok[slot] = real ? 1 : 0;
+            if (real) {
+                mbar_arrive_expect_tx(fb, SS::kPageBytes);
+                bulk_copy_g2s(ring_s + slot * SS::kPageBytes, meta_bytes + static_cast<int64_t>(phys) * SS::kPageBytes,
+                              SS::kPageBytes, fb);
+            } else {
+                svq_flag(SV_DEVERR_PAGE_TABLE);
+                mbar_arrive(fb);
+            }
+            cb = nb;
+            cp = np;
+            phys = phys_next;
+        }
+        if (!ok) svq_flag(SV_DEVERR_TIMEOUT);
         return;
     }
     const int hj = lane / SS::L, hk = lane % SS::L;
@@ -382,9 +592,9 @@ __device__ __forceinline__ void score_role(const StepArgs& a, unsigned char* rin
         const int n = pages_of(a, b, len);
         const int spp = (n + a.score_ctas - 1) / a.score_ctas;
         const int lo = min(n, c * spp), hi = min(n, lo + spp);
-        // Chunk hk + L t of kv head hj: 8 channels of kmin (chunks 0-15,
-        // coefficient Qn) or of kmax (chunks 16-31, coefficient Qp), folded
-        // from the staged queries of request b.
+        // Chunk hk + L t of kv head hj holds 8 channels of kmin (chunks 0-15,
+        // coefficient Qn = sum_h min(q_h, 0)) or of kmax (chunks 16-31,
+        // coefficient Qp = sum_h max(q_h, 0)).
         const int qb = b & 1;
         if (!failed) {
             const bool okq = mbar_wait_bounded(qfull0 + qb * 8, (static_cast<uint32_t>(b) >> 1) & 1);
@@ -417,7 +627,7 @@ __device__ __forceinline__ void score_role(const StepArgs& a, unsigned char* rin
         }
         __syncwarp();
         if (lane == 0 && !failed) mbar_arrive(qempty0 + qb * 8);
-        float* score_row = a.scores + (static_cast<int64_t>(b) * HKV + hj) * a.max_pages;
+        float* score_row = a.scores + (static_cast<int64_t>(b) * HKV + hj) * a.score_stride;
         const int first = lo + (warp - static_cast<int>(seq % kStepConsumers) + kStepConsumers) % kStepConsumers;
         for (int p = first; p < hi && !failed; p += kStepConsumers) {
             const uint32_t sq = seq + (p - lo);
@@ -436,8 +646,7 @@ __device__ __forceinline__ void score_role(const StepArgs& a, unsigned char* rin
             for (int t0 = 0; t0 < SS::C; t0 += kHalf) {
                 uint4 w[kHalf];
 #pragma unroll
-                for (int t = 0; t < kHalf; ++t)
-                    w[t] = *reinterpret_cast<const uint4*>(src + (t0 + t) * SS::L * 16);
+                for (int t = 0; t < kHalf; ++t) w[t] = *reinterpret_cast<const uint4*>(src + (t0 + t) * SS::L * 16);
 #pragma unroll
                 for (int t = 0; t < kHalf; ++t) {
                     const uint32_t x[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
@@ -457,110 +666,110 @@ __device__ __forceinline__ void score_role(const StepArgs& a, unsigned char* rin
             if (hk == 0) score_row[p] = acc;
         }
         seq += hi - lo;
-        // This warp's share of request b is written: count it (release).
+        // This warp is past request b: count it for the control warp.
         __syncwarp();
-        if (lane == 0) {
-            __threadfence();
-            atomicAdd(ctr_sdone + b, 1u);
-        }
+        if (lane == 0) red_release_cta_smem(req_done, 1u);
     }
 }
 
-// ---------------------------------------------------------------- one attention split
-// Pages [j0, j0 + my_count) of the selection of (b, g): K/V boxes by TMA into
-// the 8-stage ring (stage = sequence % 8, consumed by warp = stage), tensor-core
-// flash decode per page, merge of the 8 warps, partial (o, m, l) to the workspace.
+// ---------------------------------------------------------------- attention items
+// Page range of split `split` of the selection of (b, g).
+struct SplitRange {
+    int j0, count;
+};
+__device__ __forceinline__ SplitRange split_range(const StepArgs& a, int bg, int split, int n) {
+    const int cnt = ld_relaxed_i32(a.sel_cnt + bg);
+    const int total = max(0, min(cnt, min(a.K, n)));
+    const int chunk = (total + a.splits - 1) / a.splits;
+    const int j0 = min(total, split * chunk);
+    return {j0, min(total, j0 + chunk) - j0};
+}
+
+// Producer side of one attention item: lane group u (lanes 4u .. 4u+3) feeds
+// stage u -- the item's pages whose sequence number is u mod 8, one 2 KB box
+// per lane (K lo, K hi, V lo, V hi).  Groups run on their own (no warp-wide
+// rounds); each lane resolves its group's next page while it waits for the
+// stage of the current one.
 template <int HKV>
-__device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, int split, int n, int len,
-                                             const CUtensorMap* tmap_k, const CUtensorMap* tmap_v,
-                                             unsigned char* ring, uint32_t ring_s, uint32_t kvf0, uint32_t kve0,
-                                             int* stage_valid, uint32_t& fseq) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int bg = b * HKV + g;
-    int count;
-    {
-        int cnt;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cnt) : "l"(a.sel_cnt + bg) : "memory");
-        count = max(0, min(cnt, min(a.K, n)));
-    }
-    const int chunk = (count + a.splits - 1) / a.splits;
-    const int j0 = min(count, split * chunk);
-    const int my_count = min(count, j0 + chunk) - j0;
-    const int32_t* sel_row = a.sel_idx + static_cast<int64_t>(bg) * a.K;
-    const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
-
-    if (warp == kStepProducer) {
-        // Lane group u (lanes 4u .. 4u+3) feeds stage u: of every 8 consecutive
-        // pages it issues the one whose sequence number is u mod 8, one 2 KB
-        // box per lane (K lo, K hi, V lo, V hi).
-        const int u = lane >> 2, box = lane & 3;
-        const void* tmap = box < 2 ? static_cast<const void*>(tmap_k) : static_cast<const void*>(tmap_v);
-        auto resolve = [&](int base, int& phys_out, int& valid_out) {
-            const int ii = base + lane;
-            phys_out = -1;
-            valid_out = 0;
-            if (ii < my_count) {
-                int lp;
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(lp) : "l"(sel_row + j0 + ii) : "memory");
-                if (lp < 0 || lp >= n) {
-                    svq_flag(SV_DEVERR_SEL_IDX);
+__device__ __forceinline__ void produce_split(const StepArgs& a, const QueueItem& it, const CUtensorMap* tmap_k,
+                                              const CUtensorMap* tmap_v, uint32_t ring_s, uint32_t kvf0,
+                                              uint32_t kve0, int* stage_valid, uint32_t& fseq) {
+    const int lane = threadIdx.x & 31;
+    const int bg = it.b * HKV + it.g;
+    int len;
+    const int n = pages_of(a, it.b, len);
+    const SplitRange sr = split_range(a, bg, it.split, n);
+    const int my_count = sr.count;
+    const int32_t* sel_row = a.sel_idx + static_cast<int64_t>(bg) * a.K + sr.j0;
+    const int32_t* pt_row = a.page_table + static_cast<int64_t>(it.b) * a.max_pages;
+    const int u = lane >> 2, box = lane & 3;
+    const void* tmap = box < 2 ? static_cast<const void*>(tmap_k) : static_cast<const void*>(tmap_v);
+    // Physical page and valid rows of item page i (phys -1: skip and zero-fill).
+    auto resolve = [&](int i, int& phys_out, int& valid_out) {
+        phys_out = -1;
+        valid_out = 0;
+        if (i < my_count) {
+            const int lp = __ldcg(sel_row + i);
+            if (lp < 0 || lp >= n) {
+                svq_flag(SV_DEVERR_SEL_IDX);
+            } else {
+                const int ph = __ldg(pt_row + lp);
+                if (ph < 0 || ph >= a.num_phys_pages) {
+                    svq_flag(SV_DEVERR_PAGE_TABLE);
                 } else {
-                    const int ph = pt_row[lp];
-                    if (ph < 0 || ph >= a.num_phys_pages) {
-                        svq_flag(SV_DEVERR_PAGE_TABLE);
-                    } else {
-                        phys_out = ph;
-                        valid_out = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
-                    }
+                    phys_out = ph;
+                    valid_out = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
                 }
             }
-        };
-        int cur_phys, cur_valid, nxt_phys, nxt_valid;
-        resolve(0, cur_phys, cur_valid);
-        bool failed = false;
-        const int rot = static_cast<int>(fseq % kKvStages);
-        for (int base = 0; base < my_count && !failed; base += 32) {
-            resolve(base + 32, nxt_phys, nxt_valid);
-            for (int r8 = 0; r8 < 32 && base + r8 < my_count; r8 += 8) {
-                const int t = (u - rot + kKvStages) % kKvStages;
-                const int i = base + r8 + t;
-                const int phys = __shfl_sync(0xffffffffu, cur_phys, r8 + t);
-                const int valid = __shfl_sync(0xffffffffu, cur_valid, r8 + t);
-                bool ok = true;
-                if (i < my_count) {
-                    const uint32_t sq = fseq + i;   // sq % 8 == u
-                    if (sq >= kKvStages) ok = mbar_wait_bounded(kve0 + u * 8, ((sq / kKvStages) - 1) & 1);
-                    if (ok) {
-                        const uint32_t fb = kvf0 + u * 8;
-                        if (box == 0) {
-                            stage_valid[u] = phys >= 0 ? valid : 0;
-                            if (phys >= 0) mbar_arrive_expect_tx(fb, kKvStage);
-                            else mbar_arrive(fb);
-                        }
-                        if (phys >= 0) {
-                            const int y = static_cast<int>((static_cast<int64_t>(phys) * HKV + g) * kPage);
-                            tma_load_2d(ring_s + u * kKvStage + box * kBox, tmap, (box & 1) * 64, y, fb);
-                        }
-                    }
-                }
-                if (__any_sync(0xffffffffu, !ok)) {
-                    failed = true;
-                    break;
-                }
-            }
-            cur_phys = nxt_phys;
-            cur_valid = nxt_valid;
         }
-        if (failed && lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
-        fseq += my_count;
-        return;
+    };
+    const int first = (u - static_cast<int>(fseq % kKvStages) + kKvStages) % kKvStages;
+    int phys, valid;
+    resolve(first, phys, valid);
+    bool ok = true;
+    for (int i = first; i < my_count; i += kKvStages) {
+        int phys_next, valid_next;
+        resolve(i + kKvStages, phys_next, valid_next);
+        const uint32_t sq = fseq + i;   // sq % 8 == u
+        if (sq >= kKvStages) ok = mbar_wait_bounded(kve0 + u * 8, ((sq / kKvStages) - 1) & 1);
+        if (!ok) break;
+        const uint32_t fb = kvf0 + u * 8;
+        if (box == 0) {
+            stage_valid[u] = phys >= 0 ? valid : 0;
+            if (phys >= 0) mbar_arrive_expect_tx(fb, kKvStage);
+            else mbar_arrive(fb);
+        }
+        if (phys >= 0) {
+            const int y = static_cast<int>((static_cast<int64_t>(phys) * HKV + it.g) * kPage);
+            tma_load_2d(ring_s + u * kKvStage + box * kBox, tmap, (box & 1) * 64, y, fb);
+        }
+        phys = phys_next;
+        valid = valid_next;
     }
+    if (!ok) svq_flag(SV_DEVERR_TIMEOUT);
+    __syncwarp();
+    fseq += my_count;
+}
 
+// Compute side of one attention item: flash decode over the warp's pages
+// (stage = this warp), merge of the 8 warps through `merge`, partial (o, m, l)
+// of the split to the workspace.
+template <int HKV>
+__device__ __forceinline__ void attend_split(const StepArgs& a, const QueueItem& it, unsigned char* ring,
+                                             uint32_t ring_s, uint32_t kvf0, uint32_t kve0, const int* stage_valid,
+                                             float* merge, uint32_t& fseq) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int b = it.b, g = it.g;
+    const int bg = b * HKV + g;
+    int len;
+    const int n = pages_of(a, b, len);
+    const int my_count = split_range(a, bg, it.split, n).count;
     const int quad = lane & 3, row = lane >> 2;
     uint32_t qf[8][2];
     {
         const bool hv = row < a.group;
-        const __nv_bfloat16* qh = a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * a.group + (hv ? row : 0)) * kHeadDim;
+        const __nv_bfloat16* qh =
+            a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * a.group + (hv ? row : 0)) * kHeadDim;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             qf[kk][0] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 2 * quad) : 0u;
@@ -596,6 +805,7 @@ __device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, in
             fence_proxy_async_smem();
             __syncwarp();
         }
+        // S^T (16 tokens x 8 heads) = K (16 x 128) . Q^T, two accumulators.
         float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
@@ -644,6 +854,7 @@ __device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, in
         const uint32_t selector = (row & 1) ? 0x7632u : 0x5410u;
         const uint32_t pb0 = __byte_perm(lo0, lo1, selector);
         const uint32_t pb1 = __byte_perm(hi0, hi1, selector);
+        // O^T (128 channels x 8 heads) += V^T . P^T
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             const uint32_t addr = st_s + (2 + (mt >> 2)) * kBox + swz128(vrow, 2 * (mt & 3) + (mat & 1));
@@ -660,10 +871,8 @@ __device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, in
         l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], s2);
         l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], s2);
     }
-    // Merge the 8 consumer warps through shared memory (every stage has been
-    // consumed, so the ring is free).
-    consumers_sync();
-    float* sm_o = reinterpret_cast<float*>(ring);
+    compute_sync();   // the previous item's readers of the merge area are done
+    float* sm_o = merge;
     float* sm_m = sm_o + kStepConsumers * kMaxGroup * kHeadDim;
     float* sm_l = sm_m + kStepConsumers * kMaxGroup;
     {
@@ -683,10 +892,10 @@ __device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, in
             sm_l[warp * kMaxGroup + h1] = l_run[1];
         }
     }
-    consumers_sync();
+    compute_sync();
     const int S = a.splits;
     const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
-    for (int idx = tid; idx < a.group * kHeadDim; idx += kTopkThreadsStep) {
+    for (int idx = tid; idx < a.group * kHeadDim; idx += kComputeThreads) {
         const int h = idx / kHeadDim, d = idx % kHeadDim;
         float M = -INFINITY;
 #pragma unroll
@@ -700,35 +909,45 @@ __device__ __forceinline__ void attend_split(const StepArgs& a, int b, int g, in
                 O += sm_o[(w2 * kMaxGroup + h) * kHeadDim + d] * e;
             }
         }
-        a.o_part[((qbase + h) * S + split) * kHeadDim + d] = O;
-        if (d == 0) a.ml_part[(qbase + h) * S + split] = make_float2(M, Lsum);
+        a.o_part[((qbase + h) * S + it.split) * kHeadDim + d] = O;
+        if (d == 0) a.ml_part[(qbase + h) * S + it.split] = make_float2(M, Lsum);
     }
-    // The ring is written next by TMA: order these generic writes first.
-    fence_proxy_async_smem();
 }
 
-// Log-sum-exp combine of the splits of (b, g) into out / lse.
+// Log-sum-exp combine of the splits of (b, g) into out / lse (compute warps).
 __device__ __forceinline__ void combine_splits(const StepArgs& a, int b, int g) {
+    constexpr int kU = 8;   // splits loaded per batch
     const int S = a.splits;
     const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
-    for (int idx = threadIdx.x; idx < a.group * kHeadDim; idx += kStepThreads) {
+    for (int idx = threadIdx.x; idx < a.group * kHeadDim; idx += kComputeThreads) {
         const int h = idx / kHeadDim, d = idx % kHeadDim;
         const int64_t qh = qbase + h;
+        const float2* ml = a.ml_part + qh * S;
+        const float* op = a.o_part + qh * S * kHeadDim + d;
         float M = -INFINITY;
-        for (int s2 = 0; s2 < S; ++s2) {
-            float mx;
-            asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(mx) : "l"(a.ml_part + qh * S + s2) : "memory");
-            M = fmaxf(M, mx);
+        for (int s0 = 0; s0 < S; s0 += kU) {
+            float mx[kU];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) mx[u] = s0 + u < S ? __ldcg(&ml[s0 + u].x) : -INFINITY;
+#pragma unroll
+            for (int u = 0; u < kU; ++u) M = fmaxf(M, mx[u]);
         }
         float Lsum = 0.f, O = 0.f;
         if (M != -INFINITY) {
-            for (int s2 = 0; s2 < S; ++s2) {
-                float mx, lx, ov;
-                asm volatile("ld.relaxed.gpu.global.v2.f32 {%0, %1}, [%2];" : "=f"(mx), "=f"(lx) : "l"(a.ml_part + qh * S + s2) : "memory");
-                asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(ov) : "l"(a.o_part + (qh * S + s2) * kHeadDim + d) : "memory");
-                const float e = step_exp2(mx - M);
-                Lsum += lx * e;
-                O += ov * e;
+            for (int s0 = 0; s0 < S; s0 += kU) {
+                float2 v[kU];
+                float ov[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    v[u] = s0 + u < S ? __ldcg(&ml[s0 + u]) : make_float2(-INFINITY, 0.f);
+                    ov[u] = s0 + u < S ? __ldcg(op + (s0 + u) * kHeadDim) : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const float e = step_exp2(v[u].x - M);
+                    Lsum += v[u].y * e;
+                    O += ov[u] * e;
+                }
             }
         }
         const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
@@ -738,13 +957,6 @@ __device__ __forceinline__ void combine_splits(const StepArgs& a, int b, int g) 
 }
 
 // ---------------------------------------------------------------- the step kernel
-// Work queue, request-major: for request b, HKV selection items (one per kv
-// head) and then HKV * splits attention items.  CTAs below score_ctas first
-// score every request, then join the queue; the others take queue items from
-// the start.  A selection item waits for the scores of its request (written by
-// score CTAs, which wait on nothing); an attention item waits for a selection
-// item of a lower queue index, already taken by a running CTA.  All CTAs are
-// co-resident, so every wait ends.
 template <int HKV>
 __global__ void __launch_bounds__(kStepThreads, 2) quest_step_kernel(const __grid_constant__ StepArgs a,
                                                                    const __grid_constant__ CUtensorMap tmap_k,
@@ -757,24 +969,25 @@ __global__ void __launch_bounds__(kStepThreads, 2) quest_step_kernel(const __gri
     __shared__ __align__(8) uint64_t kv_empty[kKvStages];
     __shared__ __align__(8) uint64_t q_full[2];
     __shared__ __align__(8) uint64_t q_empty[2];
-    __shared__ __align__(128) __nv_bfloat16 qbuf[SS::kQBufBytes];   // two buffers
+    __shared__ __align__(8) uint64_t item_full[2];
+    __shared__ __align__(8) uint64_t item_empty[2];
     __shared__ unsigned char slot_ok[SS::kSlots];
     __shared__ int stage_valid[kKvStages];
-    __shared__ int s_item, s_flag;
+    __shared__ int item_slot[2];
+    __shared__ uint32_t req_done;
     __shared__ TopkScratch sc;
 
     const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int tid = threadIdx.x;
+    // Dynamic shared memory: [ring 64 KB, 1024-aligned][merge area / query buffers].
     const uint32_t raw_s = smem_addr(smem_raw);
     const uint32_t ring_s = (raw_s + 1023u) & ~1023u;   // 128-byte swizzle wants 1024-byte alignment
     unsigned char* ring = smem_raw + (ring_s - raw_s);
+    float* merge = reinterpret_cast<float*>(ring + kStepRingBytes);
     const uint32_t full0 = smem_addr(&full_bar[0]), empty0 = smem_addr(&empty_bar[0]);
     const uint32_t kvf0 = smem_addr(&kv_full[0]), kve0 = smem_addr(&kv_empty[0]);
-    const int BH = a.batch * HKV;
-    uint32_t* const ctr_next = a.ctr;
-    uint32_t* const ctr_sdone = a.ctr + 1;
-    uint32_t* const ctr_tdone = a.ctr + 1 + a.batch;
-    uint32_t* const ctr_fdone = a.ctr + 1 + a.batch + BH;
+    const uint32_t itf0 = smem_addr(&item_full[0]), ite0 = smem_addr(&item_empty[0]);
 
     if (tid == 0) {
         for (int i = 0; i < SS::kSlots; ++i) {
@@ -788,73 +1001,104 @@ __global__ void __launch_bounds__(kStepThreads, 2) quest_step_kernel(const __gri
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_addr(&q_full[i]), 1);
             mbar_init(smem_addr(&q_empty[i]), kStepConsumers);
+            mbar_init(itf0 + i * 8, 1);
+            mbar_init(ite0 + i * 8, 1 + kStepConsumers);   // producer + compute warps
         }
+        req_done = 0u;
         mbar_init_fence();
     }
-    if (warp == kStepProducer && (threadIdx.x & 31) == 0) {
+    if (warp == kStepProducer && lane == 0) {
         prefetch_tmap(&tmap_k);
         prefetch_tmap(&tmap_v);
     }
     __syncthreads();
 
-    if (static_cast<int>(blockIdx.x) < a.score_ctas) {
-        score_role<HKV>(a, ring, ring_s, full0, empty0, slot_ok, qbuf, smem_addr(qbuf), smem_addr(&q_full[0]),
-                        smem_addr(&q_empty[0]), ctr_sdone);
-        fence_proxy_async_smem();
-        __syncthreads();
-    }
-
-    const int per_req = HKV + HKV * a.splits;
-    const int n_items = a.batch * per_req;
-    const uint32_t scored = static_cast<uint32_t>(a.score_ctas) * kStepConsumers;
-    uint32_t fseq = 0;
-    for (;;) {
-        if (tid == 0) s_item = static_cast<int>(atomicAdd(ctr_next, 1u));
-        __syncthreads();
-        const int item = s_item;
-        if (item >= n_items) break;
-        const int b = item / per_req;
-        const int r = item - b * per_req;
-        int len;
-        const int n = pages_of(a, b, len);
-        if (r < HKV) {
-            // Selection of kv head r of request b.
-            const int bg = b * HKV + r;
-            if (tid == 0) {
-                if (!wait_counter(ctr_sdone + b, scored)) svq_flag(SV_DEVERR_TIMEOUT);
-                __threadfence();
-            }
-            __syncthreads();
-            if (warp != kStepProducer) {
-                step_topk(a, sc, bg, n);
-                consumers_sync();
-                if (tid == 0) {
-                    __threadfence();
-                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ctr_tdone + bg), "r"(1u) : "memory");
-                }
-            }
-        } else {
-            const int f = r - HKV;
-            const int g = f / a.splits, split = f - g * a.splits;
+    const int cta = blockIdx.x;
+    if (cta < a.score_ctas) {
+        score_role<HKV>(a, ring, ring_s, full0, empty0, slot_ok, reinterpret_cast<const __nv_bfloat16*>(merge),
+                        smem_addr(merge), smem_addr(&q_full[0]), smem_addr(&q_empty[0]), &req_done);
+    } else if (cta < a.score_ctas + a.sel_ctas && warp < kStepConsumers) {
+        const int s = cta - a.score_ctas;
+        const int g = s % HKV;
+        const int reps = a.sel_ctas / HKV;
+        for (int b = s / HKV; b < a.batch; b += reps) {
+            int len;
+            const int n = pages_of(a, b, len);
+            if (tid == 0 && !wait_counter(a.ctr + 1 + b, static_cast<uint32_t>(a.score_ctas)))
+                svq_flag(SV_DEVERR_TIMEOUT);
+            compute_sync();
             const int bg = b * HKV + g;
-            if (tid == 0) {
-                if (!wait_counter(ctr_tdone + bg, 1u)) svq_flag(SV_DEVERR_TIMEOUT);
-                __threadfence();
-            }
-            __syncthreads();
-            attend_split<HKV>(a, b, g, split, n, len, &tmap_k, &tmap_v, ring, ring_s, kvf0, kve0, stage_valid, fseq);
-            __syncthreads();
-            // The CTA that completes the last split of (b, g) combines.
-            if (tid == 0) {
-                __threadfence();
-                const uint32_t old = atomicAdd(ctr_fdone + bg, 1u);
-                s_flag = (old == static_cast<uint32_t>(a.splits) - 1u) ? 1 : 0;
-                if (s_flag) __threadfence();
-            }
-            __syncthreads();
-            if (s_flag) combine_splits(a, b, g);
+            select_row(a, sc, reinterpret_cast<float*>(ring), bg, n);
+            compute_sync();
+            if (tid == 0)
+                asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(a.ctr + 1 + a.batch + bg), "r"(1u) : "memory");
         }
-        __syncthreads();   // item boundary
+    }
+    fence_proxy_async_smem();   // generic accesses to the ring before the TMA writes below
+    __syncthreads();
+
+    // ============================================ attention queue (every CTA)
+    const int BH = a.batch * HKV;
+    uint32_t* const ctr_next = a.ctr;
+    uint32_t* const ctr_tdone = a.ctr + 1 + a.batch;
+    uint32_t* const ctr_fdone = a.ctr + 1 + a.batch + BH;
+    if (warp == kStepControl) {
+        if (lane != 0) return;
+        // Claims items one ahead of the compute warps, waits for each item's
+        // inputs and publishes it in item slot k % 2.  Retiring item j (waiting
+        // until the producer and compute warps are done with it) releases an
+        // attention item's "split done".  Before a combine item waits for the
+        // splits of its (b, g), this CTA retires all of its own items, so it
+        // never waits on a release it holds itself.
+        int kind_of[2] = {0, 0}, bg_of[2] = {0, 0};
+        uint32_t k = 0, retired = 0;
+        auto retire_next = [&]() {
+            const uint32_t j = retired++;
+            const int s = j & 1;
+            if (!mbar_wait_bounded(ite0 + s * 8, (j >> 1) & 1)) svq_flag(SV_DEVERR_TIMEOUT);
+            if (kind_of[s] == 1) red_release_gpu(ctr_fdone + bg_of[s], 1u);
+        };
+        for (;;) {
+            const int item = static_cast<int>(atomicAdd(ctr_next, 1u));
+            const QueueItem it = decode_item<HKV>(a, item);
+            while (retired + 2 <= k) retire_next();       // slot k % 2 must be free
+            if (it.kind == 2)
+                while (retired < k) retire_next();
+            const int bg = it.b * HKV + it.g;
+            if (it.kind == 1 && !wait_counter(ctr_tdone + bg, 1u)) svq_flag(SV_DEVERR_TIMEOUT);
+            if (it.kind == 2 && !wait_counter(ctr_fdone + bg, static_cast<uint32_t>(a.splits)))
+                svq_flag(SV_DEVERR_TIMEOUT);
+            const int s = k & 1;
+            item_slot[s] = it.kind == 0 ? -1 : item;
+            kind_of[s] = it.kind;
+            bg_of[s] = bg;
+            mbar_arrive(itf0 + s * 8);
+            ++k;
+            if (it.kind == 0) break;
+        }
+        while (retired + 1 < k) retire_next();            // everything before the stop marker
+        return;
+    }
+    uint32_t fseq = 0;   // K/V pages this CTA has streamed (stage = fseq % 8)
+    for (uint32_t k = 0;; ++k) {
+        const int s = k & 1;
+        if (!wait_item(itf0 + s * 8, (k >> 1) & 1)) {
+            svq_flag(SV_DEVERR_TIMEOUT);
+            break;
+        }
+        const int item = item_slot[s];
+        const QueueItem it = decode_item<HKV>(a, item);
+        if (it.kind == 1) {
+            if (warp == kStepProducer)
+                produce_split<HKV>(a, it, &tmap_k, &tmap_v, ring_s, kvf0, kve0, stage_valid, fseq);
+            else
+                attend_split<HKV>(a, it, ring, ring_s, kvf0, kve0, stage_valid, merge, fseq);
+        } else if (it.kind == 2 && warp != kStepProducer) {
+            combine_splits(a, it.b, it.g);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(ite0 + s * 8);
+        if (it.kind == 0) break;
     }
 }
 
@@ -889,26 +1133,22 @@ bool step_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
 
 struct StepLayout {
     size_t scores, o_part, ml_part, ctr, total;
-    int splits;
+    int splits, stride;
 };
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-#ifndef SVQ_STEP_PAGES_PER_SPLIT
-#define SVQ_STEP_PAGES_PER_SPLIT 16
-#endif
-#ifndef SVQ_STEP_SCORE_PERMILLE
-#define SVQ_STEP_SCORE_PERMILLE 0   // 0: CTAs split by the bytes each role reads
-#endif
+constexpr int kStepSmem = 1024 + kStepRingBytes + kMergeBytes;   // alignment slack + ring + merge area
 
 StepLayout step_layout(int batch, int num_q_heads, int num_kv_heads, int max_pages, int budget_pages) {
     StepLayout L;
     const int kb = min(budget_pages, max_pages);
     L.splits = max(1, min(kStepMaxSplits, (kb + SVQ_STEP_PAGES_PER_SPLIT - 1) / SVQ_STEP_PAGES_PER_SPLIT));
+    L.stride = (max_pages + 31) / 32 * 32;
     const size_t bh = static_cast<size_t>(batch) * num_kv_heads;
     const size_t heads = static_cast<size_t>(batch) * num_q_heads * L.splits;
     L.scores = 0;
-    L.o_part = align256(bh * max_pages * sizeof(float));
+    L.o_part = align256(bh * L.stride * sizeof(float));
     L.ml_part = L.o_part + align256(heads * kHeadDim * sizeof(float));
     L.ctr = L.ml_part + align256(heads * sizeof(float2));
     L.total = L.ctr + align256((1 + batch + 2 * bh) * sizeof(uint32_t));
@@ -950,22 +1190,18 @@ int launch_step_hkv(const sv_cache* c, const void* q, int num_q_heads, const int
     if (!step_pool_map(&tmap_k, c->k_pool, rows) || !step_pool_map(&tmap_v, c->v_pool, rows)) return SV_ERR_CUDA;
 
     const int grid = per_sm * sm_count;
-    int score_ctas;
-    if (SVQ_STEP_SCORE_PERMILLE > 0) {
-        score_ctas = static_cast<int>(static_cast<int64_t>(grid) * SVQ_STEP_SCORE_PERMILLE / 1000);
-    } else {
-        // Metadata bytes per request vs selected K/V bytes per request.
-        const double score_b = static_cast<double>(max_pages) * HKV * 2 * kHeadDim * 2;
-        const double attend_b = static_cast<double>(min(budget_pages, max_pages)) * HKV * 2 * kPage * kHeadDim * 2;
-        score_ctas = static_cast<int>(grid * score_b / (score_b + attend_b) + 0.5);
-    }
-    score_ctas = max(1, min(grid, score_ctas));
+    const int sel_ctas = HKV * max(1, min(batch, SVQ_STEP_SELECTORS_PER_HEAD));
+    if (grid < sel_ctas + 1) return SV_ERR_UNSUPPORTED;
+    // Score CTAs take the first wave (one per SM, so every score CTA streams at
+    // the same rate); selectors and attention-only CTAs the rest.
+    int score_ctas = sm_count;
+    if (SVQ_STEP_SCORE_PERMILLE > 0) score_ctas = static_cast<int>(static_cast<int64_t>(grid) * SVQ_STEP_SCORE_PERMILLE / 1000);
+    score_ctas = max(1, min(grid - sel_ctas, score_ctas));
 
     unsigned char* ws = static_cast<unsigned char*>(workspace);
     StepArgs a;
     a.meta = static_cast<const __nv_bfloat16*>(c->meta);
     a.num_phys_pages = c->num_phys_pages;
-    a.num_kv_heads = c->num_kv_heads;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.num_q_heads = num_q_heads;
     a.group = num_q_heads / c->num_kv_heads;
@@ -976,6 +1212,7 @@ int launch_step_hkv(const sv_cache* c, const void* q, int num_q_heads, const int
     a.K = budget_pages;
     a.scale_log2 = softmax_scale * 1.4426950408889634f;
     a.scores = reinterpret_cast<float*>(ws + Ly.scores);
+    a.score_stride = Ly.stride;
     a.sel_idx = sel_idx;
     a.sel_cnt = sel_cnt;
     a.o_part = reinterpret_cast<float*>(ws + Ly.o_part);
@@ -983,6 +1220,7 @@ int launch_step_hkv(const sv_cache* c, const void* q, int num_q_heads, const int
     a.out = static_cast<__nv_bfloat16*>(out);
     a.lse = lse;
     a.score_ctas = score_ctas;
+    a.sel_ctas = sel_ctas;
     a.splits = Ly.splits;
     a.ctr = reinterpret_cast<uint32_t*>(ws + Ly.ctr);
 
