@@ -262,7 +262,6 @@ constexpr int kTopkThreads = SVQ_TOPK_THREADS;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kRadixBins = 2048;
 constexpr int kBinsPerThread = kRadixBins / kTopkThreads;
-constexpr int kLoadItems = 8;
 constexpr int kCandCap = 256;
 static_assert(kRadixBins % kTopkThreads == 0 && kTopkWarps <= 32, "top-K block shape");
 

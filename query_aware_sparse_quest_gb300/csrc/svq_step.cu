@@ -31,6 +31,7 @@
 #include <cudaTypedefs.h>
 
 #include "svq_common.cuh"
+#include "svq_topk.cuh"
 
 namespace svq {
 
@@ -45,16 +46,14 @@ constexpr int kStepRingBytes = 64 * 1024;
 constexpr int kBox = kPage * 64 * 2;                       // 16 x 64 bf16 TMA box (2 KB)
 constexpr int kKvStage = 4 * kBox;                         // K lo | K hi | V lo | V hi
 constexpr int kKvStages = kStepRingBytes / kKvStage;       // 8: stage s is consumed by warp s
-constexpr int kTopkItems = 32;                             // keys per thread
-constexpr int kStepMaxPages = kComputeThreads * kTopkItems;  // 8192 pages (131072 tokens) per request
-constexpr int kStepBins = 2048;
-constexpr int kStepCandCap = 256;
+constexpr int kStepMaxPages = kRowMaxPages;               // 8192 pages (131072 tokens) per request
 constexpr int kStepMaxSplits = 64;
 constexpr uint32_t kSpinLimit = 1u << 24;                  // polls of a cross-CTA counter before giving up
 // Merge area for the eight warps' partial outputs: o [8][8 heads][128] + m, l [8][8].
 constexpr int kMergeBytes = kStepConsumers * kMaxGroup * (kHeadDim + 2) * 4;
 static_assert(kKvStages == kStepConsumers, "each ring stage belongs to one compute warp");
 static_assert(kStepMaxPages * 4 <= kStepRingBytes, "a score row must fit the ring for the top-K");
+static_assert(kComputeThreads == kRowThreads, "the compute warps run the row top-K");
 
 #ifndef SVQ_STEP_PAGES_PER_SPLIT
 #define SVQ_STEP_PAGES_PER_SPLIT 16
@@ -104,11 +103,6 @@ __device__ __forceinline__ float step_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-// Order-preserving map of a float to u32 (larger float -> larger key).
-__device__ __forceinline__ uint32_t step_order_key(float f) {
-    const uint32_t u = __float_as_uint(f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 // 128-byte swizzle of a 16 x 64 bf16 box (chunk = 16 bytes).
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
@@ -221,250 +215,11 @@ __device__ __forceinline__ QueueItem decode_item(const StepArgs& a, int item) {
     return it;
 }
 
-// ---------------------------------------------------------------- top-K of one score row (256 compute threads)
-// Keeps the m = min(K, n) highest scores (ties to the lower page index) and
-// writes their indices in ascending order.  The row is staged through shared
-// memory with coalesced loads; thread t then holds keys 32t .. 32t+31.  A
-// lower bound on the m-th largest key (the smallest j-th largest key over
-// threads, for the smallest j in 1..4 with enough keys at or above it) trims
-// the adaptive histogram to the top of the row; the boundary bin's keys are
-// ranked exactly (radix passes when the bin holds more than 256 keys); the
-// compaction follows the index order.
-struct TopkScratch {
-    uint32_t hist[kStepBins];
-    uint32_t warp_tot[kStepConsumers];
-    uint32_t warp_red[6][kStepConsumers];
-    uint32_t cand_key[kStepCandCap];
-    int32_t cand_idx[kStepCandCap];
-    uint32_t bin, rem, cand, T, take;
-};
-
-__device__ void select_row(const StepArgs& a, TopkScratch& sc, float* stage, int bg, int n) {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = a.K;
-    const int m = min(K, n);
-    int32_t* out = a.sel_idx + static_cast<int64_t>(bg) * K;
-    if (n <= K) {
-        for (int i = tid; i < K; i += kComputeThreads) out[i] = i < n ? i : -1;
-        if (tid == 0) a.sel_cnt[bg] = n < 0 ? 0 : n;
-        return;
-    }
-    // Coalesced 16-byte loads -> swizzled shared memory -> 32 consecutive keys per thread.
-    const float* row = a.scores + static_cast<int64_t>(bg) * a.score_stride;
-#pragma unroll
-    for (int e = 0; e < kTopkItems / 4; ++e) {
-        const int idx = 4 * tid + 4 * kComputeThreads * e;
-        const float4 v = idx < a.score_stride ? __ldcg(reinterpret_cast<const float4*>(row + idx))
-                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        const int owner = (tid >> 3) + (kComputeThreads / 8) * e;
-        const int chunk = tid & 7;
-        *reinterpret_cast<float4*>(stage + owner * 32 + 4 * (chunk ^ (owner & 7))) = v;
-    }
-    compute_sync();
-    const int i0 = kTopkItems * tid;
-    uint32_t key[kTopkItems];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        const float4 v = *reinterpret_cast<const float4*>(stage + tid * 32 + 4 * (c ^ (tid & 7)));
-        key[4 * c] = step_order_key(v.x);
-        key[4 * c + 1] = step_order_key(v.y);
-        key[4 * c + 2] = step_order_key(v.z);
-        key[4 * c + 3] = step_order_key(v.w);
-    }
-    // Row minimum / maximum and, per thread, the maxima of its four groups of
-    // 8 keys sorted (q1 >= q2 >= q3 >= q4): the thread holds at least j keys
-    // >= qj, one from each of j groups.
-    uint32_t kmin = 0xffffffffu, kmax = 0u;
-    uint32_t qmax[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-    for (int e = 0; e < kTopkItems; ++e) {
-        const bool v = i0 + e < n;
-        kmin = min(kmin, v ? key[e] : 0xffffffffu);
-        qmax[e >> 3] = max(qmax[e >> 3], v ? key[e] : 0u);
-    }
-    kmax = max(max(qmax[0], qmax[1]), max(qmax[2], qmax[3]));
-    {
-        uint32_t x;
-#define SVQ_CSWAP(i, j) x = min(qmax[i], qmax[j]); qmax[i] = max(qmax[i], qmax[j]); qmax[j] = x;
-        SVQ_CSWAP(0, 1) SVQ_CSWAP(2, 3) SVQ_CSWAP(0, 2) SVQ_CSWAP(1, 3) SVQ_CSWAP(1, 2)
-#undef SVQ_CSWAP
-    }
-    const bool full = i0 + kTopkItems <= n;   // only threads with 32 valid keys give bounds
-    uint32_t red[6] = {kmin, kmax, full ? qmax[0] : 0xffffffffu, full ? qmax[1] : 0xffffffffu,
-                       full ? qmax[2] : 0xffffffffu, full ? qmax[3] : 0xffffffffu};
-    for (int i = tid; i < kStepBins; i += kComputeThreads) sc.hist[i] = 0u;
-#pragma unroll
-    for (int r = 0; r < 6; ++r) {
-        const uint32_t v = r == 1 ? __reduce_max_sync(0xffffffffu, red[r]) : __reduce_min_sync(0xffffffffu, red[r]);
-        if (lane == 0) sc.warp_red[r][warp] = v;
-    }
-    compute_sync();
-#pragma unroll
-    for (int r = 0; r < 6; ++r) {
-        const uint32_t v = lane < kStepConsumers ? sc.warp_red[r][lane] : (r == 1 ? 0u : 0xffffffffu);
-        red[r] = r == 1 ? __reduce_max_sync(0xffffffffu, v) : __reduce_min_sync(0xffffffffu, v);
-    }
-    // Lower bound on the m-th largest key: the full threads each hold j keys
-    // >= the minimum over them of qj, so that minimum is a bound once
-    // j * (number of full threads) >= m; the smallest such j gives the tightest.
-    uint32_t lo = red[0];
-    const int full_threads = min(kComputeThreads, n / kTopkItems);
-#pragma unroll
-    for (int j = 4; j >= 1; --j)
-        if (j * full_threads >= m) lo = red[1 + j];
-    const uint32_t hi = red[1];
-    const uint32_t range = hi - lo;
-    const int rbits = range == 0 ? 0 : 32 - __clz(range);
-    const uint32_t shift = rbits > 11 ? rbits - 11 : 0;
-#pragma unroll
-    for (int e = 0; e < kTopkItems; ++e)
-        if (i0 + e < n && key[e] >= lo) atomicAdd(&sc.hist[(key[e] - lo) >> shift], 1u);
-    compute_sync();
-    auto find_bin = [&](uint32_t remaining) {
-        constexpr int kBpt = kStepBins / kComputeThreads;
-        const uint32_t top = kStepBins - 1 - kBpt * tid;
-        uint32_t cnt[kBpt];
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < kBpt; ++i) {
-            cnt[i] = sc.hist[top - i];
-            sum += cnt[i];
-        }
-        uint32_t v = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += t;
-        }
-        if (lane == 31) sc.warp_tot[warp] = v;
-        compute_sync();
-        uint32_t add = 0;
-        for (int w2 = 0; w2 < warp; ++w2) add += sc.warp_tot[w2];
-        uint32_t before = v + add - sum;
-#pragma unroll
-        for (int i = 0; i < kBpt; ++i) {
-            if (before < remaining && remaining <= before + cnt[i]) {
-                sc.bin = top - i;
-                sc.rem = remaining - before;
-            }
-            before += cnt[i];
-        }
-        compute_sync();
-    };
-    find_bin(static_cast<uint32_t>(m));
-    const uint32_t bstar = sc.bin, need = sc.rem;
-    uint32_t T, take;
-    if (sc.hist[bstar] <= kStepCandCap) {
-        // Keys of the boundary bin: per-thread mask, positions by a block scan.
-        uint32_t cmask = 0;
-#pragma unroll
-        for (int e = 0; e < kTopkItems; ++e)
-            cmask |= ((i0 + e < n && key[e] >= lo && ((key[e] - lo) >> shift) == bstar) ? 1u : 0u) << e;
-        const uint32_t cnt = __popc(cmask);
-        uint32_t incl = cnt;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        if (lane == 31) sc.warp_tot[warp] = incl;
-        compute_sync();
-        uint32_t pos = incl - cnt;
-        uint32_t total = 0;
-#pragma unroll
-        for (int w2 = 0; w2 < kStepConsumers; ++w2) {
-            const uint32_t t = sc.warp_tot[w2];
-            pos += w2 < warp ? t : 0u;
-            total += t;
-        }
-#pragma unroll
-        for (int e = 0; e < kTopkItems; ++e) {   // static indices keep key[] in registers
-            if ((cmask >> e) & 1u) {
-                sc.cand_key[pos] = key[e];
-                sc.cand_idx[pos] = i0 + e;
-                ++pos;
-            }
-        }
-        if (tid == 0) sc.cand = total;
-        compute_sync();
-        const int nc = static_cast<int>(sc.cand);
-        if (tid < nc) {
-            const uint32_t my_k = sc.cand_key[tid];
-            const int my_i = sc.cand_idx[tid];
-            uint32_t above = 0, tied_before = 0;
-            for (int j = 0; j < nc; ++j) {
-                const uint32_t kj = sc.cand_key[j];
-                above += kj > my_k;
-                tied_before += (kj == my_k && sc.cand_idx[j] < my_i);
-            }
-            if (above + tied_before == need - 1) {
-                sc.T = my_k;
-                sc.take = need - above;
-            }
-        }
-        compute_sync();
-        T = sc.T;
-        take = sc.take;
-    } else {
-        // Radix select on the full keys: 11 + 11 + 10 bits.
-        uint32_t prefix = 0, remaining = static_cast<uint32_t>(m);
-        for (int pass = 0; pass < 3; ++pass) {
-            const int sh = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-            const int nbits = pass == 2 ? 10 : 11;
-            const uint32_t nbins = 1u << nbits;
-            const uint32_t hi_mask = pass == 0 ? 0u : ~((1u << (sh + nbits)) - 1u);
-            compute_sync();
-            for (int i = tid; i < kStepBins; i += kComputeThreads) sc.hist[i] = 0u;
-            compute_sync();
-#pragma unroll
-            for (int e = 0; e < kTopkItems; ++e)
-                if (i0 + e < n && (key[e] & hi_mask) == prefix) atomicAdd(&sc.hist[(key[e] >> sh) & (nbins - 1u)], 1u);
-            compute_sync();
-            find_bin(remaining);
-            prefix |= sc.bin << sh;
-            remaining = sc.rem;
-        }
-        T = prefix;
-        take = remaining;
-    }
-    uint32_t gt_mask = 0, eq_mask = 0;
-#pragma unroll
-    for (int e = 0; e < kTopkItems; ++e) {
-        if (i0 + e < n) {
-            gt_mask |= (key[e] > T ? 1u : 0u) << e;
-            eq_mask |= (key[e] == T ? 1u : 0u) << e;
-        }
-    }
-    const uint32_t packed = (static_cast<uint32_t>(__popc(gt_mask)) << 16) | __popc(eq_mask);
-    uint32_t v = packed;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += t;
-    }
-    if (lane == 31) sc.warp_tot[warp] = v;
-    compute_sync();
-    uint32_t add = 0;
-    for (int w2 = 0; w2 < warp; ++w2) add += sc.warp_tot[w2];
-    const uint32_t excl = v + add - packed;
-    const uint32_t eq_before = excl & 0xffffu;
-    uint32_t sel_mask = gt_mask;
-    uint32_t eq_take = take > eq_before ? min(take - eq_before, static_cast<uint32_t>(__popc(eq_mask))) : 0u;
-    uint32_t eqm = eq_mask;
-    while (eq_take--) {
-        const uint32_t low = eqm & (0u - eqm);
-        sel_mask |= low;
-        eqm ^= low;
-    }
-    uint32_t pos = (excl >> 16) + min(eq_before, take);
-    while (sel_mask) {
-        const int e = __ffs(sel_mask) - 1;
-        sel_mask &= sel_mask - 1u;
-        if (pos < static_cast<uint32_t>(m)) out[pos] = i0 + e;
-        ++pos;
-    }
-    for (int i = m + tid; i < K; i += kComputeThreads) out[i] = -1;
-    if (tid == 0) a.sel_cnt[bg] = m;
+// ---------------------------------------------------------------- top-K of one score row
+// (svq_topk.cuh; the compute warps are threads 0 .. 255, barrier 1)
+__device__ __forceinline__ void select_row(const StepArgs& a, RowTopkScratch& sc, float* stage, int bg, int n) {
+    topk_row_256<1, true>(a.scores + static_cast<int64_t>(bg) * a.score_stride, n, a.K,
+                          a.sel_idx + static_cast<int64_t>(bg) * a.K, a.sel_cnt + bg, sc, stage);
 }
 
 // ---------------------------------------------------------------- score role
@@ -975,7 +730,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) quest_step_kernel(const __gri
     __shared__ int stage_valid[kKvStages];
     __shared__ int item_slot[2];
     __shared__ uint32_t req_done;
-    __shared__ TopkScratch sc;
+    __shared__ RowTopkScratch sc;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
