@@ -45,7 +45,12 @@ def _load():
         lib.oracle_update_meta.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, i64]
         lib.oracle_select.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, P, P, P]
         lib.oracle_decode.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, f32, P, P]
-        for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode):
+        lib.oracle_select_ex.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i64, i32, i32, i32,
+                                         P, P, P]
+        lib.oracle_decode_ex.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, i32, f32,
+                                         P, P]
+        for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode, lib.oracle_select_ex,
+                  lib.oracle_decode_ex):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -87,22 +92,26 @@ def update_meta(cache: Cache, k_new: np.ndarray, v_new: np.ndarray, slot_mapping
 
 
 def select(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
-           budget_pages: int) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
-    """Returns (sel_idx [B][Hkv][K] int32, sel_cnt [B][Hkv] int32, scores [B][Hkv][max_pages] fp32).
+           budget_pages: int, per_q_head: bool = False, sink_pages: int = 0,
+           window_pages: int = 0) -> Tuple[np.ndarray, np.ndarray, np.ndarray]:
+    """Returns (sel_idx [B][R][K] int32, sel_cnt [B][R] int32, scores [B][R][max_pages] fp32),
+    R = num_q_heads when per_q_head, else num_kv_heads.
 
-    Score entries past a request's last page are NaN."""
+    Score entries past a request's last page are NaN; forced (sink / window)
+    pages keep their bound as the score."""
     q = _c(q, np.uint16)
     page_table = _c(page_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
     B, Hq, D = q.shape
+    R = Hq if per_q_head else cache.Hkv
     max_pages = page_table.shape[1]
     K = int(budget_pages)
-    sel_idx = np.empty((B, cache.Hkv, K), dtype=np.int32)
-    sel_cnt = np.empty((B, cache.Hkv), dtype=np.int32)
-    scores = np.full((B, cache.Hkv, max_pages), np.nan, dtype=np.float32)
-    rc = _load().oracle_select(_ptr(q), _ptr(cache.meta), _ptr(page_table), _ptr(seq_lens), B, Hq,
-                               cache.Hkv, D, cache.P, max_pages, K, cache.n_phys, _ptr(sel_idx),
-                               _ptr(sel_cnt), _ptr(scores))
+    sel_idx = np.empty((B, R, K), dtype=np.int32)
+    sel_cnt = np.empty((B, R), dtype=np.int32)
+    scores = np.full((B, R, max_pages), np.nan, dtype=np.float32)
+    rc = _load().oracle_select_ex(_ptr(q), _ptr(cache.meta), _ptr(page_table), _ptr(seq_lens), B, Hq,
+                                  cache.Hkv, D, cache.P, max_pages, K, cache.n_phys, int(bool(per_q_head)),
+                                  int(sink_pages), int(window_pages), _ptr(sel_idx), _ptr(sel_cnt), _ptr(scores))
     if rc != 0:
         raise ValueError(f"oracle_select failed ({rc})")
     return sel_idx, sel_cnt, scores
@@ -110,8 +119,9 @@ def select(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
 
 def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
            sel_idx: Optional[np.ndarray] = None, sel_cnt: Optional[np.ndarray] = None,
-           scale: Optional[float] = None) -> Tuple[np.ndarray, np.ndarray]:
-    """Returns (out fp32 [B][Hq][D], lse fp32 [B][Hq]); dense when sel_idx is None."""
+           scale: Optional[float] = None, per_q_head: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """Returns (out fp32 [B][Hq][D], lse fp32 [B][Hq]); dense when sel_idx is None.
+    With per_q_head, sel_idx has one row per query head."""
     q = _c(q, np.uint16)
     page_table = _c(page_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
@@ -126,9 +136,9 @@ def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
         K = sel_idx.shape[2]
     out = np.empty((B, Hq, D), dtype=np.float32)
     lse = np.empty((B, Hq), dtype=np.float32)
-    rc = _load().oracle_decode(_ptr(q), _ptr(cache.k), _ptr(cache.v), _ptr(page_table), _ptr(seq_lens),
-                               B, Hq, cache.Hkv, D, cache.P, max_pages, cache.n_phys, _ptr(sel_idx),
-                               _ptr(sel_cnt), K, float(scale), _ptr(out), _ptr(lse))
+    rc = _load().oracle_decode_ex(_ptr(q), _ptr(cache.k), _ptr(cache.v), _ptr(page_table), _ptr(seq_lens),
+                                  B, Hq, cache.Hkv, D, cache.P, max_pages, cache.n_phys, _ptr(sel_idx),
+                                  _ptr(sel_cnt), K, int(bool(per_q_head)), float(scale), _ptr(out), _ptr(lse))
     if rc != 0:
         raise ValueError(f"oracle_decode failed ({rc})")
     return out, lse

@@ -19,6 +19,15 @@
  *    ties going to the lower page index; exact softmax attention runs over
  *    only those pages.
  *
+ * Selection options (the pages describe none of them; the readings taken):
+ *  - per_q_head: every query head selects its own pages by its own bound
+ *    (no sum over the kv group); sel_idx then has one row per query head and
+ *    each head attends only its row's pages.
+ *  - sink_pages / window_pages: the first sink_pages and the last
+ *    window_pages logical pages of a request are always kept.  They rank
+ *    above every other page, among themselves by lower page index, and they
+ *    count toward the budget K.
+ *
  * It is written literally: the score uses the max-form above (not any
  * rearrangement of it), ranking is a full sort, attention is two passes
  * over an explicit score vector.  Accumulation is fp32 in the loop order
@@ -123,12 +132,16 @@ static float page_bound(const uint16_t* q_group, int G, int D,
 typedef struct {
     float score;
     int32_t page;
+    int32_t forced;   /* 1: a sink or window page */
 } scored_page;
 
-/* Higher score first; equal scores: lower logical page index first. */
+/* Forced pages first, among themselves by lower index; then higher score first,
+ * equal scores: lower logical page index first. */
 static int by_score_then_index(const void* pa, const void* pb) {
     const scored_page* a = (const scored_page*)pa;
     const scored_page* b = (const scored_page*)pb;
+    if (a->forced != b->forced) return a->forced ? -1 : 1;
+    if (a->forced) return (a->page < b->page) ? -1 : (a->page > b->page);   /* forced: by index alone */
     if (a->score > b->score) return -1;
     if (a->score < b->score) return 1;
     return (a->page < b->page) ? -1 : (a->page > b->page);
@@ -140,62 +153,83 @@ static int by_int_ascending(const void* pa, const void* pb) {
 }
 
 /*
- * For every request b and kv group g: score each of the request's
- * n_b = ceil(len_b / P) logical pages, keep the min(K, n_b) best under the
- * order (score desc, page asc), and emit their logical indices ascending.
- * scores (nullable) receives [B][Hkv][max_pages] fp32, entries past n_b untouched.
+ * For every request b and selection row r -- kv group r, or query head r when
+ * per_q_head -- score each of the request's n_b = ceil(len_b / P) logical
+ * pages with the bound of the row's query heads (the group's G heads, or the
+ * one head) against the metadata of the row's kv head, keep the min(K, n_b)
+ * first pages under the order (forced desc, score desc, page asc), and emit
+ * their logical indices ascending.  R = per_q_head ? Hq : Hkv rows.
+ * scores (nullable) receives [B][R][max_pages] fp32 (the bound, also for
+ * forced pages), entries past n_b untouched.
  */
-int oracle_select(const uint16_t* q, const uint16_t* meta,
-                  const int32_t* page_table, const int32_t* seq_lens,
-                  int B, int Hq, int Hkv, int D, int P, int max_pages, int K,
-                  int64_t n_phys, int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
-    if (Hq % Hkv != 0 || K < 1) return -1;
+int oracle_select_ex(const uint16_t* q, const uint16_t* meta,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     int B, int Hq, int Hkv, int D, int P, int max_pages, int K,
+                     int64_t n_phys, int per_q_head, int sink_pages, int window_pages,
+                     int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
+    if (Hq % Hkv != 0 || K < 1 || sink_pages < 0 || window_pages < 0) return -1;
     const int G = Hq / Hkv;
+    const int R = per_q_head ? Hq : Hkv;
     scored_page* list = (scored_page*)malloc((size_t)max_pages * sizeof(scored_page));
     if (!list) return -1;
     for (int b = 0; b < B; ++b) {
         int n = (seq_lens[b] + P - 1) / P;
         if (n < 1 || n > max_pages) { free(list); return -2; }
-        for (int g = 0; g < Hkv; ++g) {
-            const uint16_t* qg = q + ((size_t)b * Hq + (size_t)g * G) * D;
+        for (int r = 0; r < R; ++r) {
+            const int g = per_q_head ? r / G : r;
+            const int first_head = per_q_head ? r : g * G;
+            const int heads = per_q_head ? 1 : G;
+            const uint16_t* qr = q + ((size_t)b * Hq + (size_t)first_head) * D;
             for (int p = 0; p < n; ++p) {
                 int64_t phys = page_table[(size_t)b * max_pages + p];
                 if (phys < 0 || phys >= n_phys) { free(list); return -2; }
                 const uint16_t* kmin = meta + (((size_t)phys * Hkv + g) * 2 + 0) * D;
                 const uint16_t* kmax = meta + (((size_t)phys * Hkv + g) * 2 + 1) * D;
-                list[p].score = page_bound(qg, G, D, kmin, kmax);
+                list[p].score = page_bound(qr, heads, D, kmin, kmax);
                 list[p].page = p;
-                if (scores) scores[((size_t)b * Hkv + g) * max_pages + p] = list[p].score;
+                list[p].forced = (p < sink_pages || p >= n - window_pages) ? 1 : 0;
+                if (scores) scores[((size_t)b * R + r) * max_pages + p] = list[p].score;
             }
             qsort(list, (size_t)n, sizeof(scored_page), by_score_then_index);
             int m = n < K ? n : K;
-            int32_t* out = sel_idx + ((size_t)b * Hkv + g) * K;
+            int32_t* out = sel_idx + ((size_t)b * R + r) * K;
             for (int j = 0; j < m; ++j) out[j] = list[j].page;
             qsort(out, (size_t)m, sizeof(int32_t), by_int_ascending);
             for (int j = m; j < K; ++j) out[j] = -1;
-            sel_cnt[(size_t)b * Hkv + g] = m;
+            sel_cnt[(size_t)b * R + r] = m;
         }
     }
     free(list);
     return 0;
 }
 
+/* The base method: one row per kv group, no forced pages. */
+int oracle_select(const uint16_t* q, const uint16_t* meta,
+                  const int32_t* page_table, const int32_t* seq_lens,
+                  int B, int Hq, int Hkv, int D, int P, int max_pages, int K,
+                  int64_t n_phys, int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
+    return oracle_select_ex(q, meta, page_table, seq_lens, B, Hq, Hkv, D, P, max_pages, K, n_phys, 0, 0, 0,
+                            sel_idx, sel_cnt, scores);
+}
+
 /*
  * Exact softmax attention of every query head over the tokens of a page
  * list: all n_b logical pages when sel_idx is NULL (dense), else the
- * sel_cnt[b][g] pages of sel_idx[b][g].  The last logical page n_b - 1 holds
+ * sel_cnt[b][r] pages of sel_idx[b][r], r = the head's kv group g, or the
+ * head itself when per_q_head (sel_idx then has Hq rows per request).  The last logical page n_b - 1 holds
  * len_b - P*(n_b - 1) tokens; every other page holds P.
  *   z_t = (q . k_t) * scale;  m = max z;  l = sum exp(z - m);
  *   out = sum exp(z_t - m) v_t / l;  lse = m + ln(l).
  * out is fp32 [B][Hq][D]; lse fp32 [B][Hq].
  */
-int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
-                  const int32_t* page_table, const int32_t* seq_lens,
-                  int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
-                  const int32_t* sel_idx, const int32_t* sel_cnt, int K, float scale,
-                  float* out, float* lse) {
+int oracle_decode_ex(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                     const int32_t* page_table, const int32_t* seq_lens,
+                     int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
+                     const int32_t* sel_idx, const int32_t* sel_cnt, int K, int per_q_head, float scale,
+                     float* out, float* lse) {
     if (Hq % Hkv != 0) return -1;
     const int G = Hq / Hkv;
+    const int R = per_q_head ? Hq : Hkv;
     float* z = (float*)malloc((size_t)max_pages * P * sizeof(float));
     int32_t* tok_page = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
     int32_t* tok_off = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
@@ -207,12 +241,13 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_p
         if (n < 1 || n > max_pages) { rc = -2; break; }
         for (int h = 0; h < Hq && rc == 0; ++h) {
             int g = h / G;
-            int count = sel_idx ? sel_cnt[(size_t)b * Hkv + g] : n;
+            int r = per_q_head ? h : g;
+            int count = sel_idx ? sel_cnt[(size_t)b * R + r] : n;
             if (count < 0 || count > (sel_idx ? K : n)) { rc = -2; break; }
             /* Gather the attended tokens as (physical page, offset). */
             int ntok = 0;
             for (int j = 0; j < count; ++j) {
-                int p = sel_idx ? sel_idx[((size_t)b * Hkv + g) * K + j] : j;
+                int p = sel_idx ? sel_idx[((size_t)b * R + r) * K + j] : j;
                 if (p < 0 || p >= n) { rc = -2; break; }
                 int64_t phys = page_table[(size_t)b * max_pages + p];
                 if (phys < 0 || phys >= n_phys) { rc = -2; break; }
@@ -254,4 +289,14 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_p
     free(tok_page);
     free(tok_off);
     return rc;
+}
+
+/* The base method: one selection row per kv group. */
+int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                  const int32_t* page_table, const int32_t* seq_lens,
+                  int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
+                  const int32_t* sel_idx, const int32_t* sel_cnt, int K, float scale,
+                  float* out, float* lse) {
+    return oracle_decode_ex(q, k_pool, v_pool, page_table, seq_lens, B, Hq, Hkv, D, P, max_pages, n_phys,
+                            sel_idx, sel_cnt, K, 0, scale, out, lse);
 }

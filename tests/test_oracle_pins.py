@@ -323,3 +323,98 @@ def test_needle_pages_rank_high():
             s = scores[b, g, :1000]
             pct.append(float((s > s[p]).mean()))
     assert np.mean(pct) < 0.25, np.mean(pct)
+
+
+# ---------------------------------------------------------------- selection options
+
+def _tiny_integer_case(rng, G, Hkv=1):
+    D, P = int(rng.integers(1, 5)), int(rng.integers(1, 4))
+    n = int(rng.integers(1, 11))
+    L = (n - 1) * P + int(rng.integers(1, P + 1))
+    k = bf(rng.integers(-3, 4, size=(L, Hkv, D)).astype(np.float64))
+    q = bf(rng.integers(-2, 3, size=(1, G * Hkv, D)).astype(np.float64))
+    phys = rng.permutation(n).astype(np.int32)
+    cache = oracle.Cache(n, Hkv, P, D, fill_bits=0)
+    pos = np.arange(L)
+    oracle.update_meta(cache, k, k, (phys[pos // P] * P + pos % P).astype(np.int32))
+    return cache, q, phys, L, n, P, bf16_bits_to_f32(k).astype(np.float64), bf16_bits_to_f32(q).astype(np.float64)[0]
+
+
+def _best_subset(scores, m, candidates):
+    """Lexicographically smallest m-subset of `candidates` with the largest score sum."""
+    return max(itertools.combinations(candidates, m), key=lambda c: (sum(scores[i] for i in c), [-i for i in c]))
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_per_q_head_selection_matches_bruteforce(seed):
+    """Per-query-head selection: each head's scores are its own box bound and
+    its page set is the best K-subset under that head's scores alone."""
+    rng = np.random.default_rng(300 + seed)
+    G = int(rng.integers(1, 4))
+    cache, q, phys, L, n, P, kf, qf = _tiny_integer_case(rng, G)
+    K = int(rng.integers(1, n + 2))
+    sel, cnt, sc = oracle.select(cache, q, phys[None], np.array([L], np.int32), K, per_q_head=True)
+    assert sel.shape == (1, G, K)
+    m = min(K, n)
+    for h in range(G):
+        s = [box_bound_bruteforce(qf[h : h + 1], kf[p * P : min(L, (p + 1) * P), 0]) for p in range(n)]
+        np.testing.assert_allclose(sc[0, h, :n], s, rtol=0, atol=0)
+        assert cnt[0, h] == m
+        assert sel[0, h, :m].tolist() == list(_best_subset(s, m, range(n)))
+
+
+def test_per_q_head_with_one_head_per_group_equals_group_selection():
+    wl = synth.make_workload(_tiny_spec(num_q_heads=2, num_kv_heads=2, ctx=60, seed=21))
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    a = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, 4)
+    b = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, 4, per_q_head=True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_sink_and_window_pages_always_kept(seed):
+    """Forced pages: the first S and last W pages rank first (lower index first
+    among them); the rest of the budget is the best subset of the other pages."""
+    rng = np.random.default_rng(400 + seed)
+    cache, q, phys, L, n, P, kf, qf = _tiny_integer_case(rng, G=2)
+    K = int(rng.integers(1, n + 2))
+    S, W = int(rng.integers(0, 3)), int(rng.integers(0, 3))
+    sel, cnt, sc = oracle.select(cache, q, phys[None], np.array([L], np.int32), K, sink_pages=S, window_pages=W)
+    s = [box_bound_bruteforce(qf, kf[p * P : min(L, (p + 1) * P), 0]) for p in range(n)]
+    np.testing.assert_allclose(sc[0, 0, :n], s, rtol=0, atol=0)   # scores stay the bound
+    forced = [p for p in range(n) if p < S or p >= n - W]
+    others = [p for p in range(n) if p not in forced]
+    m = min(K, n)
+    keep = forced[:m]
+    keep += list(_best_subset(s, m - len(keep), others)) if m > len(keep) else []
+    assert cnt[0, 0] == m
+    assert sel[0, 0, :m].tolist() == sorted(keep)
+    assert sel[0, 0, m:].tolist() == [-1] * (K - m)
+
+
+def test_per_q_head_decode_matches_sdpa_per_head():
+    """Attention with one page list per query head equals, head by head, fp64
+    scaled-dot-product attention over that head's pages; with every head of a
+    group given the group's list it equals group-row attention."""
+    wl = synth.make_workload(_tiny_spec(num_q_heads=4, num_kv_heads=2, ctx=70, seed=31, head_dim=8))
+    cache = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    sel, cnt, _ = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, 3, per_q_head=True)
+    scale = 0.3
+    out, lse = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, sel, cnt, scale=scale, per_q_head=True)
+    P, G = wl.spec.page_size, 2
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    for b in range(wl.spec.batch):
+        k, v = request_keys(wl, b)
+        for h in range(4):
+            toks = np.concatenate([np.arange(p * P, min(int(wl.seq_lens[b]), (p + 1) * P))
+                                   for p in sel[b, h, : cnt[b, h]]])
+            o_ref, l_ref = _sdpa_fp64(qf[b, h : h + 1], k[toks, h // G], v[toks, h // G], scale)
+            np.testing.assert_allclose(out[b, h], o_ref[0], rtol=2e-5, atol=2e-6)
+            np.testing.assert_allclose(lse[b, h], l_ref[0], rtol=2e-6, atol=2e-6)
+    gsel, gcnt, _ = oracle.select(cache, wl.q, wl.page_table, wl.seq_lens, 3)
+    rep_sel, rep_cnt = np.repeat(gsel, G, axis=1), np.repeat(gcnt, G, axis=1)
+    o1, l1 = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, rep_sel, rep_cnt, scale=scale, per_q_head=True)
+    o2, l2 = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, gsel, gcnt, scale=scale)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
