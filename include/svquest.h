@@ -158,6 +158,58 @@ size_t sv_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32
                                        int32_t pages);
 
 /*
+ * Selection options (the pages describe none of these policies; each is a
+ * switch on the selection, off when zero):
+ *   per_q_head    0: one page set per kv head, scored with the bound summed
+ *                 over its query heads (the base method);
+ *                 1: one page set per query head, scored with that head's
+ *                 own bound against its kv head's metadata.  sel_idx then
+ *                 holds R = num_q_heads rows per request ([B][Hq][K],
+ *                 sel_cnt [B][Hq], scores [B][Hq][max_pages]) and each
+ *                 query head attends only its own row's pages.
+ *   sink_pages,   the first sink_pages and the last window_pages logical
+ *   window_pages  pages of every request are always selected: they rank
+ *                 above every scored page, among themselves by lower page
+ *                 index, and count toward budget_pages.  Their entries in
+ *                 scores_out are +inf.
+ *   layer,        a layer with layer < dense_layers attends densely:
+ *   dense_layers  sv_quest_select_ex returns SV_OK without launching or
+ *                 writing anything, and sv_sparse_decode_ex ignores sel_idx
+ *                 and reads every page.
+ * Negative values, or per_q_head other than 0 / 1, are SV_ERR_INVALID_ARG.
+ * A NULL opts pointer means all zero.
+ */
+typedef struct sv_quest_opts {
+    int32_t per_q_head;
+    int32_t sink_pages;
+    int32_t window_pages;
+    int32_t layer;
+    int32_t dense_layers;
+} sv_quest_opts;
+
+/* sv_quest_select with options; R = num_q_heads rows per request when
+ * per_q_head, else num_kv_heads.  The scores workspace (when scores_out is
+ * NULL) is sv_quest_select_ex_workspace_size(...) bytes. */
+int sv_quest_select_ex(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                       const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                       int32_t max_pages, int32_t budget_pages, const sv_quest_opts* opts,
+                       int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+size_t sv_quest_select_ex_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t max_pages, const sv_quest_opts* opts);
+
+/* sv_sparse_decode with options: sel_idx / sel_cnt in the layout
+ * sv_quest_select_ex wrote for the same options; batch * R <= 65535.  The
+ * workspace is sv_sparse_decode_workspace_size(...) bytes, as without options. */
+int sv_sparse_decode_ex(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                        const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                        int32_t max_pages, const int32_t* sel_idx, const int32_t* sel_cnt,
+                        int32_t budget_pages, const sv_quest_opts* opts, float softmax_scale,
+                        void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
  * sv_sparse_decode_static_scratch -- sv_sparse_decode without a caller
  * workspace; the paper has no counterpart to this call.  It is for callers
  * that cannot allocate device memory: plugins inside a host framework that

@@ -26,6 +26,11 @@ class SvError(RuntimeError):
         self.status = status
 
 
+class sv_quest_opts(ctypes.Structure):
+    _fields_ = [("per_q_head", ctypes.c_int32), ("sink_pages", ctypes.c_int32), ("window_pages", ctypes.c_int32),
+                ("layer", ctypes.c_int32), ("dense_layers", ctypes.c_int32)]
+
+
 class sv_cache(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("meta", ctypes.c_void_p),
                 ("num_phys_pages", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
@@ -46,6 +51,7 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     cp = ctypes.POINTER(sv_cache)
+    op = ctypes.POINTER(sv_quest_opts)
     sig = {
         "sv_quest_update_meta": [cp, vp, vp, vp, i64, vp],
         "sv_quest_score": [cp, vp, i32, vp, vp, i32, i32, vp, vp],
@@ -54,6 +60,8 @@ def _load():
         "sv_sparse_decode": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp, sz, vp],
         "sv_sparse_decode_static_scratch": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp],
         "sv_quest_decode_step": [cp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
+        "sv_quest_select_ex": [cp, vp, i32, vp, vp, i32, i32, i32, op, vp, vp, vp, vp, sz, vp],
+        "sv_sparse_decode_ex": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, op, f32, vp, vp, vp, sz, vp],
         "sv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int],
     }
     for name, args in sig.items():
@@ -66,6 +74,8 @@ def _load():
     lib.sv_sparse_decode_workspace_size.restype = sz
     lib.sv_quest_decode_step_workspace_size.argtypes = [i32, i32, i32, i32, i32]
     lib.sv_quest_decode_step_workspace_size.restype = sz
+    lib.sv_quest_select_ex_workspace_size.argtypes = [i32, i32, i32, i32, op]
+    lib.sv_quest_select_ex_workspace_size.restype = sz
     lib.sv_status_string.argtypes = [ctypes.c_int]
     lib.sv_status_string.restype = ctypes.c_char_p
     lib.sv_version.argtypes = []
@@ -199,6 +209,42 @@ def sv_quest_decode_step(cache: Cache, q: torch.Tensor, page_table: torch.Tensor
     _check("sv_quest_decode_step", _load().sv_quest_decode_step(
         cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
         scale, _p(sel_idx), _p(sel_cnt), _p(out), _p(lse), _p(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def quest_opts(per_q_head: bool = False, sink_pages: int = 0, window_pages: int = 0, layer: int = 0,
+               dense_layers: int = 0) -> sv_quest_opts:
+    return sv_quest_opts(int(bool(per_q_head)), int(sink_pages), int(window_pages), int(layer), int(dense_layers))
+
+
+def sv_quest_select_ex_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_pages: int,
+                                      opts: Optional[sv_quest_opts] = None) -> int:
+    return int(_load().sv_quest_select_ex_workspace_size(batch, num_q_heads, num_kv_heads, max_pages,
+                                                         None if opts is None else ctypes.byref(opts)))
+
+
+def sv_quest_select_ex(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                       budget_pages: int, opts: Optional[sv_quest_opts], sel_idx: torch.Tensor,
+                       sel_cnt: torch.Tensor, scores_out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    B, Hq, _ = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("sv_quest_select_ex", _load().sv_quest_select_ex(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
+        None if opts is None else ctypes.byref(opts), _p(sel_idx), _p(sel_cnt), _p(scores_out), _p(workspace),
+        ws_bytes, _stream(stream)))
+
+
+def sv_sparse_decode_ex(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
+                        sel_idx: Optional[torch.Tensor], sel_cnt: Optional[torch.Tensor],
+                        opts: Optional[sv_quest_opts], out: torch.Tensor, lse: torch.Tensor,
+                        workspace: torch.Tensor, softmax_scale: Optional[float] = None, stream=None) -> None:
+    B, Hq, D = q.shape
+    K = 0 if sel_idx is None else int(sel_idx.shape[2])
+    scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
+    _check("sv_sparse_decode_ex", _load().sv_sparse_decode_ex(
+        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
+        _p(sel_cnt), K, None if opts is None else ctypes.byref(opts), scale, _p(out), _p(lse), _p(workspace),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

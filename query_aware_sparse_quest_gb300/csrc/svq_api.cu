@@ -12,14 +12,14 @@ int read_error_decode(uint32_t* flags, int reset);
 int launch_update_meta(const sv_cache* c, const void* k_new, const void* v_new, const int32_t* slot_mapping,
                        int64_t num_tokens, cudaStream_t stream);
 int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
-                 const int32_t* seq_lens, int batch, int max_pages, float* scores, int sm_count,
-                 cudaStream_t stream);
+                 const int32_t* seq_lens, int batch, int max_pages, bool per_q_head, int sink, int window,
+                 float* scores, int sm_count, cudaStream_t stream);
 int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
                 int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, cudaStream_t stream);
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
-                  const int32_t* sel_cnt, int budget_pages, float softmax_scale, void* out, float* lse,
-                  void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream);
+                  const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
+                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream);
 int decode_max_splits(int pages);
 size_t decode_workspace_bytes(int batch, int num_q_heads, int splits);
 int read_error_step(uint32_t* flags, int reset);
@@ -74,8 +74,70 @@ int check_batch(const void* q, const int32_t* page_table, const int32_t* seq_len
     return SV_OK;
 }
 
-size_t scores_bytes(int batch, int num_kv_heads, int max_pages) {
-    return (static_cast<size_t>(batch) * num_kv_heads * max_pages * sizeof(float) + 255) / 256 * 256;
+size_t scores_bytes(int batch, int rows_per_req, int max_pages) {
+    return (static_cast<size_t>(batch) * rows_per_req * max_pages * sizeof(float) + 255) / 256 * 256;
+}
+
+const sv_quest_opts kBaseOpts = {0, 0, 0, 0, 0};
+
+int check_opts(const sv_quest_opts* o) {
+    if (o->per_q_head != 0 && o->per_q_head != 1) return SV_ERR_INVALID_ARG;
+    if (o->sink_pages < 0 || o->window_pages < 0 || o->layer < 0 || o->dense_layers < 0) return SV_ERR_INVALID_ARG;
+    return SV_OK;
+}
+
+int rows_per_request(const sv_cache* c, int num_q_heads, const sv_quest_opts* o) {
+    return o->per_q_head ? num_q_heads : c->num_kv_heads;
+}
+
+int select_impl(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                const sv_quest_opts* opts, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, void* workspace,
+                size_t workspace_bytes, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if ((st = check_opts(opts))) return st;
+    if (!sel_idx || !sel_cnt || budget_pages < 1) return SV_ERR_INVALID_ARG;
+    if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
+    if (opts->layer < opts->dense_layers) return SV_OK;   // dense layer: no selection
+    const int rows = rows_per_request(cache, num_q_heads, opts);
+    float* scores = scores_out;
+    if (!scores) {
+        if (!workspace || workspace_bytes < scores_bytes(batch, rows, max_pages)) return SV_ERR_WORKSPACE;
+        scores = static_cast<float*>(workspace);
+    }
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, opts->per_q_head != 0,
+                           opts->sink_pages, opts->window_pages, scores, sms, s)))
+        return st;
+    return launch_topk(scores, seq_lens, batch, rows, max_pages, budget_pages, sel_idx, sel_cnt, s);
+}
+
+int decode_impl(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                const int32_t* seq_lens, int32_t batch, int32_t max_pages, const int32_t* sel_idx,
+                const int32_t* sel_cnt, int32_t budget_pages, const sv_quest_opts* opts, float softmax_scale,
+                void* out, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+    int st = check_cache(cache);
+    if (st) return st;
+    if ((st = check_heads(cache, num_q_heads))) return st;
+    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
+    if ((st = check_opts(opts))) return st;
+    if (!out || !lse) return SV_ERR_INVALID_ARG;
+    if (opts->layer < opts->dense_layers) sel_idx = nullptr;   // dense layer: every page
+    if (sel_idx && (!sel_cnt || budget_pages < 1)) return SV_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
+    const int rows = sel_idx ? rows_per_request(cache, num_q_heads, opts) : cache->num_kv_heads;
+    if (static_cast<int64_t>(batch) * rows > 65535) return SV_ERR_UNSUPPORTED;
+    if (!workspace) return SV_ERR_WORKSPACE;
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
+                         budget_pages, opts->per_q_head != 0, softmax_scale, out, lse, workspace, workspace_bytes,
+                         sms, static_cast<cudaStream_t>(stream));
 }
 
 }  // namespace
@@ -105,7 +167,7 @@ int sv_quest_score(const sv_cache* cache, const void* q, int32_t num_q_heads, co
     if (!scores) return SV_ERR_INVALID_ARG;
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
-    return launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms,
+    return launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms,
                         static_cast<cudaStream_t>(stream));
 }
 
@@ -128,24 +190,23 @@ int sv_quest_select(const sv_cache* cache, const void* q, int32_t num_q_heads, c
                     const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
                     int32_t* sel_idx, int32_t* sel_cnt, float* scores_out, void* workspace,
                     size_t workspace_bytes, void* stream) {
-    int st = check_cache(cache);
-    if (st) return st;
-    if ((st = check_heads(cache, num_q_heads))) return st;
-    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
-    if (!sel_idx || !sel_cnt || budget_pages < 1) return SV_ERR_INVALID_ARG;
-    if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
-    float* scores = scores_out;
-    if (!scores) {
-        if (!workspace || workspace_bytes < scores_bytes(batch, cache->num_kv_heads, max_pages))
-            return SV_ERR_WORKSPACE;
-        scores = static_cast<float*>(workspace);
-    }
-    int sms = 0;
-    if ((st = sm_count_of_current_device(&sms))) return st;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms, s)))
-        return st;
-    return launch_topk(scores, seq_lens, batch, cache->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, s);
+    return select_impl(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, &kBaseOpts,
+                       sel_idx, sel_cnt, scores_out, workspace, workspace_bytes, stream);
+}
+
+int sv_quest_select_ex(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                       const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                       const sv_quest_opts* opts, int32_t* sel_idx, int32_t* sel_cnt, float* scores_out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+    return select_impl(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages,
+                       opts ? opts : &kBaseOpts, sel_idx, sel_cnt, scores_out, workspace, workspace_bytes, stream);
+}
+
+size_t sv_quest_select_ex_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t max_pages, const sv_quest_opts* opts) {
+    if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_pages < 1) return 0;
+    const bool per_head = opts && opts->per_q_head;
+    return scores_bytes(batch, per_head ? num_q_heads : num_kv_heads, max_pages);
 }
 
 size_t sv_sparse_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t pages) {
@@ -157,20 +218,17 @@ int sv_sparse_decode(const sv_cache* cache, const void* q, int32_t num_q_heads, 
                      const int32_t* seq_lens, int32_t batch, int32_t max_pages, const int32_t* sel_idx,
                      const int32_t* sel_cnt, int32_t budget_pages, float softmax_scale, void* out, float* lse,
                      void* workspace, size_t workspace_bytes, void* stream) {
-    int st = check_cache(cache);
-    if (st) return st;
-    if ((st = check_heads(cache, num_q_heads))) return st;
-    if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
-    if (!out || !lse) return SV_ERR_INVALID_ARG;
-    if (sel_idx && (!sel_cnt || budget_pages < 1)) return SV_ERR_INVALID_ARG;
-    if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
-    if (static_cast<int64_t>(batch) * cache->num_kv_heads > 65535) return SV_ERR_UNSUPPORTED;
-    if (!workspace) return SV_ERR_WORKSPACE;
-    int sms = 0;
-    if ((st = sm_count_of_current_device(&sms))) return st;
-    return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                         budget_pages, softmax_scale, out, lse, workspace, workspace_bytes, sms,
-                         static_cast<cudaStream_t>(stream));
+    return decode_impl(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt, budget_pages,
+                       &kBaseOpts, softmax_scale, out, lse, workspace, workspace_bytes, stream);
+}
+
+int sv_sparse_decode_ex(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                        const int32_t* seq_lens, int32_t batch, int32_t max_pages, const int32_t* sel_idx,
+                        const int32_t* sel_cnt, int32_t budget_pages, const sv_quest_opts* opts,
+                        float softmax_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                        void* stream) {
+    return decode_impl(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt, budget_pages,
+                       opts ? opts : &kBaseOpts, softmax_scale, out, lse, workspace, workspace_bytes, stream);
 }
 
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -207,11 +265,12 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
     // Two-stage path: scores at the front of the workspace, split-K partials after.
     const size_t sb = scores_bytes(batch, cache->num_kv_heads, max_pages);
     float* scores = static_cast<float*>(workspace);
-    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, scores, sms, s))) return st;
+    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s)))
+        return st;
     if ((st = launch_topk(scores, seq_lens, batch, cache->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, s)))
         return st;
     return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                         budget_pages, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
+                         budget_pages, false, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
                          workspace_bytes - sb, sms, s);
 }
 

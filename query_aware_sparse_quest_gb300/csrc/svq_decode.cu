@@ -36,7 +36,9 @@ struct DecodeArgs {
     int num_kv_heads;
     const __nv_bfloat16* q;
     int num_q_heads;
-    int group;
+    int group;                // query heads of one selection row
+    int rows_per_req;         // selection rows per request (kv heads, or query heads)
+    int kv_div;               // selection row r reads kv head r / kv_div
     const int32_t* page_table;
     const int32_t* seq_lens;
     int max_pages;
@@ -83,9 +85,10 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
     __shared__ __align__(8) uint64_t empty_bar[kStages];
 
     const int split = blockIdx.x;
-    const int bg = blockIdx.y;
-    const int b = bg / a.num_kv_heads;
-    const int g = bg % a.num_kv_heads;
+    const int bg = blockIdx.y;                 // selection row of the whole batch
+    const int b = bg / a.rows_per_req;
+    const int g = bg % a.rows_per_req;          // row in the request: query heads g * group ..
+    const int kvh = g / a.kv_div;               // kv head the row reads
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const uint32_t raw_s = smem_addr(smem_raw);
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
                             else mbar_arrive(fb);
                         }
                         if (phys >= 0) {
-                            const int y = static_cast<int>((static_cast<int64_t>(phys) * a.num_kv_heads + g) * kPage);
+                            const int y = static_cast<int>((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * kPage);
                             tma_load_2d(dst, tmap, (box & 1) * 64, y, fb);
                         }
                         last = i;
@@ -464,8 +467,8 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
 
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
-                  const int32_t* sel_cnt, int budget_pages, float softmax_scale, void* out, float* lse,
-                  void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream) {
+                  const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
+                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream) {
     static bool attr_set[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
@@ -480,7 +483,11 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
                                                       kDecodeSmem) != cudaSuccess || per_sm < 1)
         return SV_ERR_CUDA;
     const int pages = sel_idx ? budget_pages : max_pages;
-    const int bh = batch * c->num_kv_heads;
+    // Selection rows: one per kv head (its query heads share the page list),
+    // or one per query head.  Dense decode always works per kv head.
+    const bool per_head = per_q_head && sel_idx;
+    const int rows_per_req = per_head ? num_q_heads : c->num_kv_heads;
+    const int bh = batch * rows_per_req;
     int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm) / bh);
     splits = max(1, min(splits, decode_max_splits(pages)));
     if (decode_workspace_bytes(batch, num_q_heads, splits) > workspace_bytes) return SV_ERR_WORKSPACE;
@@ -496,7 +503,9 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     a.num_kv_heads = c->num_kv_heads;
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.num_q_heads = num_q_heads;
-    a.group = num_q_heads / c->num_kv_heads;
+    a.group = per_head ? 1 : num_q_heads / c->num_kv_heads;
+    a.rows_per_req = rows_per_req;
+    a.kv_div = per_head ? num_q_heads / c->num_kv_heads : 1;
     a.page_table = page_table;
     a.seq_lens = seq_lens;
     a.max_pages = max_pages;

@@ -61,11 +61,19 @@ struct ScoreShape {
 // k, k + L, ... of that head's 512-byte [kmin | kmax] row, so a page's score
 // is one register accumulation per lane plus a log2(L)-level shuffle sum;
 // the warp then releases the slot on its "empty" mbarrier.
-template <int HKV>
+//
+// PER_HEAD: one score row per query head (no sum over the group): lane (u, k)
+// = (lane / 4, lane % 4) scores query head u of every kv head j over channels
+// 32k .. 32k+31 with the bound's per-channel form, q >= 0 ? q kmax : q kmin
+// (the larger of the two products), and the four channel quarters are summed
+// by two shuffles.  Rows are [B][Hkv * group][max_pages].
+// Forced pages (the first `sink` and last `window` pages of a request) get
+// the score +inf, which the top-K ranks first, ties to the lower index.
+template <int HKV, bool PER_HEAD>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const __nv_bfloat16* __restrict__ meta, int64_t num_phys_pages, const __nv_bfloat16* __restrict__ q,
     int group, const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens, int max_pages,
-    int pages_per_cta, float* __restrict__ scores) {
+    int pages_per_cta, int sink, int window, float* __restrict__ scores) {
     using S = ScoreShape<HKV>;
     constexpr int kSlots = S::kSlots, L = S::L, C = S::C;
     extern __shared__ __align__(128) unsigned char ring[];
@@ -160,6 +168,63 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     }
 
     // ---------------- consumer warps
+    auto forced = [&](int lp) { return lp < sink || lp >= n - window; };
+    if constexpr (PER_HEAD) {
+        const int u = lane >> 2, kq = lane & 3;
+        const bool active = u < group;
+        uint4 qreg[HKV][4];   // query head u of kv head j, channels 32 kq .. 32 kq + 31
+#pragma unroll
+        for (int j = 0; j < HKV; ++j) {
+            const __nv_bfloat16* qrow = qstage + (j * group + (active ? u : 0)) * kHeadDim + kq * 32;
+#pragma unroll
+            for (int t = 0; t < 4; ++t) qreg[j][t] = *reinterpret_cast<const uint4*>(qrow + t * 8);
+        }
+        const int rows = HKV * group;
+        for (int p = warp; p < span; p += kScoreConsumers) {
+            const int slot = p % kSlots;
+            const bool okw = mbar_wait_bounded(full0 + slot * 8, (p / kSlots) & 1);
+            if (__any_sync(0xffffffffu, !okw)) {
+                if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
+                break;
+            }
+            const unsigned char* page = ring + slot * S::kPageBytes;
+            float acc[HKV];
+#pragma unroll
+            for (int j = 0; j < HKV; ++j) {
+                const unsigned char* mrow = page + j * 512 + kq * 64;   // kmin at +0, kmax at +256
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint4 mn = *reinterpret_cast<const uint4*>(mrow + t * 16);
+                    const uint4 mx = *reinterpret_cast<const uint4*>(mrow + 256 + t * 16);
+                    const uint32_t a[4] = {mn.x, mn.y, mn.z, mn.w};
+                    const uint32_t bb[4] = {mx.x, mx.y, mx.z, mx.w};
+                    const uint32_t c4[4] = {qreg[j][t].x, qreg[j][t].y, qreg[j][t].z, qreg[j][t].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float q0 = bf16lo(c4[e]), q1 = bf16hi(c4[e]);
+                        s0 = fmaf(q0, q0 >= 0.f ? bf16lo(bb[e]) : bf16lo(a[e]), s0);
+                        s1 = fmaf(q1, q1 >= 0.f ? bf16hi(bb[e]) : bf16hi(a[e]), s1);
+                    }
+                }
+                acc[j] = s0 + s1;
+            }
+            const bool real = slot_ok[slot] != 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + slot * 8);
+            const int lp = cta_begin + p;
+            const bool f = forced(lp);
+#pragma unroll
+            for (int j = 0; j < HKV; ++j) {
+                float v = acc[j] + __shfl_xor_sync(0xffffffffu, acc[j], 1);
+                v += __shfl_xor_sync(0xffffffffu, v, 2);
+                if (kq == 0 && active)
+                    scores[(static_cast<int64_t>(b) * rows + j * group + u) * max_pages + lp] =
+                        f ? INFINITY : (real ? v : 0.f);
+            }
+        }
+        return;
+    }
     const int hj = lane / L;        // kv head of this lane
     const int hk = lane % L;        // first chunk of this lane
     float c[C][8];
@@ -198,20 +263,20 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         float acc = real ? a0 + a1 : 0.f;
 #pragma unroll
         for (int m = 1; m < L; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (hk == 0) score_row[p] = acc;
+        if (hk == 0) score_row[p] = forced(cta_begin + p) ? INFINITY : acc;
     }
 }
 
-template <int HKV>
+template <int HKV, bool PER_HEAD>
 int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const int32_t* page_table,
-                     const int32_t* seq_lens, int batch, int max_pages, float* scores, int sm_count,
-                     cudaStream_t stream) {
+                     const int32_t* seq_lens, int batch, int max_pages, int sink, int window, float* scores,
+                     int sm_count, cudaStream_t stream) {
     using S = ScoreShape<HKV>;
     static bool attr_set[64] = {};
     const int dev = current_device();
     if (dev < 0) return SV_ERR_CUDA;
     if (dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(score_pages_kernel<HKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(score_pages_kernel<HKV, PER_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  S::kSmemBytes) != cudaSuccess)
             return SV_ERR_CUDA;
         if (dev < 64) attr_set[dev] = true;
@@ -220,25 +285,32 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
     int64_t ppc = (static_cast<int64_t>(batch) * max_pages + sm_count - 1) / sm_count;
     if (ppc < 32) ppc = 32;
     const int ctas = ceil_div(max_pages, ppc);
-    const cudaError_t e = launch_pdl(score_pages_kernel<HKV>, dim3(ctas, batch), dim3(kScoreThreads),
+    const cudaError_t e = launch_pdl(score_pages_kernel<HKV, PER_HEAD>, dim3(ctas, batch), dim3(kScoreThreads),
                                      S::kSmemBytes, stream, static_cast<const __nv_bfloat16*>(c->meta),
                                      c->num_phys_pages, q, group, page_table, seq_lens, max_pages,
-                                     static_cast<int>(ppc), scores);
+                                     static_cast<int>(ppc), sink, window, scores);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
-                 const int32_t* seq_lens, int batch, int max_pages, float* scores, int sm_count,
-                 cudaStream_t stream) {
+                 const int32_t* seq_lens, int batch, int max_pages, bool per_q_head, int sink, int window,
+                 float* scores, int sm_count, cudaStream_t stream) {
     const int group = num_q_heads / c->num_kv_heads;
     const auto* qq = static_cast<const __nv_bfloat16*>(q);
+#define SVQ_SCORE_CASE(H)                                                                                      \
+    case H:                                                                                                    \
+        return per_q_head ? launch_score_hkv<H, true>(c, qq, group, page_table, seq_lens, batch, max_pages,   \
+                                                      sink, window, scores, sm_count, stream)                 \
+                          : launch_score_hkv<H, false>(c, qq, group, page_table, seq_lens, batch, max_pages,  \
+                                                       sink, window, scores, sm_count, stream);
     switch (c->num_kv_heads) {
-        case 1: return launch_score_hkv<1>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, sm_count, stream);
-        case 2: return launch_score_hkv<2>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, sm_count, stream);
-        case 4: return launch_score_hkv<4>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, sm_count, stream);
-        case 8: return launch_score_hkv<8>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, sm_count, stream);
+        SVQ_SCORE_CASE(1)
+        SVQ_SCORE_CASE(2)
+        SVQ_SCORE_CASE(4)
+        SVQ_SCORE_CASE(8)
         default: return SV_ERR_UNSUPPORTED;
     }
+#undef SVQ_SCORE_CASE
 }
 
 // ---------------------------------------------------------------- top-K

@@ -165,3 +165,31 @@ def test_decode_step_rejects_bad_args(lib):
     need = binding.sv_quest_decode_step_workspace_size(8, 32, 4, 100, 16)
     assert call(ws_bytes=need - 1) == SV_ERR_WORKSPACE
     assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
+
+
+def test_select_ex_and_decode_ex_option_checks(lib):
+    c = ctypes.byref(_fake_cache())
+
+    def sel(opts, ws_bytes=1 << 30):
+        return lib.sv_quest_select_ex(c, FAKE, 32, FAKE, FAKE, 8, 100, 16, ctypes.byref(opts), FAKE, FAKE, None,
+                                      FAKE, ws_bytes, None)
+
+    def dec(opts, batch=8, sel=FAKE):
+        return lib.sv_sparse_decode_ex(c, FAKE, 32, FAKE, FAKE, batch, 100, sel, FAKE, 16, ctypes.byref(opts),
+                                       0.088, FAKE, FAKE, FAKE, 1 << 30, None)
+    for bad in (binding.quest_opts(sink_pages=-1), binding.quest_opts(window_pages=-2),
+                binding.quest_opts(layer=-1), binding.quest_opts(dense_layers=-1)):
+        assert sel(bad) == SV_ERR_INVALID_ARG
+        assert dec(bad) == SV_ERR_INVALID_ARG
+    two = binding.quest_opts()
+    two.per_q_head = 2
+    assert sel(two) == SV_ERR_INVALID_ARG
+    # A dense layer selects nothing: returns SV_OK before any launch.
+    assert sel(binding.quest_opts(layer=1, dense_layers=2)) == SV_OK
+    # Per-query-head rows: 2100 requests x 32 query heads exceed the 65535 grid rows.
+    assert dec(binding.quest_opts(per_q_head=True), batch=2100) == SV_ERR_UNSUPPORTED
+    # per-head scores need Hq rows of workspace
+    need = binding.sv_quest_select_ex_workspace_size(8, 32, 4, 100, binding.quest_opts(per_q_head=True))
+    assert need == 8 * 32 * 100 * 4
+    assert sel(binding.quest_opts(per_q_head=True), ws_bytes=need - 1) == SV_ERR_WORKSPACE
+    assert binding.sv_quest_select_ex_workspace_size(8, 32, 4, 100, None) == 8 * 4 * 100 * 4
