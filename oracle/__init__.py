@@ -49,8 +49,15 @@ def _load():
                                          P, P, P]
         lib.oracle_decode_ex.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, i32, f32,
                                          P, P]
+        lib.oracle_quantize_rows.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, P, i64]
+        lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, i32,
+                                          f32, P, P]
+        lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_value.restype = f32
+        lib.oracle_e4m3_encode.argtypes = [f32]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode, lib.oracle_select_ex,
-                  lib.oracle_decode_ex):
+                  lib.oracle_decode_ex, lib.oracle_quantize_rows, lib.oracle_decode_fp8):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -67,15 +74,25 @@ def _c(a: np.ndarray, dtype) -> np.ndarray:
 
 
 class Cache:
-    """Host copy of a paged pool: k/v [n_phys][Hkv][P][D] and meta [n_phys][Hkv][2][D]."""
+    """Host copy of a paged pool: k/v [n_phys][Hkv][P][D] and meta [n_phys][Hkv][2][D].
+
+    With fp8, the pool also holds e4m3 codes k8/v8 [n_phys][Hkv][P][D] and fp32
+    row scales ks/vs [n_phys][Hkv][P] (k/v then keep the appended bf16 rows,
+    from which the metadata is computed)."""
 
     def __init__(self, n_phys: int, num_kv_heads: int, page_size: int = 16, head_dim: int = 128,
-                 fill_bits: int = 0):
+                 fill_bits: int = 0, fp8: bool = False, fill_code: int = 0, fill_scale: float = 0.0):
         shape = (n_phys, num_kv_heads, page_size, head_dim)
         self.k = np.full(shape, fill_bits, dtype=np.uint16)
         self.v = np.full(shape, fill_bits, dtype=np.uint16)
         self.meta = np.zeros((n_phys, num_kv_heads, 2, head_dim), dtype=np.uint16)
         self.n_phys, self.Hkv, self.P, self.D = n_phys, num_kv_heads, page_size, head_dim
+        self.fp8 = fp8
+        if fp8:
+            self.k8 = np.full(shape, fill_code, dtype=np.uint8)
+            self.v8 = np.full(shape, fill_code, dtype=np.uint8)
+            self.ks = np.full(shape[:3], fill_scale, dtype=np.float32)
+            self.vs = np.full(shape[:3], fill_scale, dtype=np.float32)
 
 
 def update_meta(cache: Cache, k_new: np.ndarray, v_new: np.ndarray, slot_mapping: np.ndarray) -> None:
@@ -89,6 +106,20 @@ def update_meta(cache: Cache, k_new: np.ndarray, v_new: np.ndarray, slot_mapping
                                     _ptr(slot_mapping), T)
     if rc != 0:
         raise ValueError(f"oracle_update_meta failed ({rc})")
+    if cache.fp8:
+        rc = _load().oracle_quantize_rows(_ptr(cache.k8), _ptr(cache.v8), _ptr(cache.ks), _ptr(cache.vs),
+                                          cache.n_phys, cache.Hkv, cache.P, cache.D, _ptr(k_new), _ptr(v_new),
+                                          _ptr(slot_mapping), T)
+        if rc != 0:
+            raise ValueError(f"oracle_quantize_rows failed ({rc})")
+
+
+def e4m3_value(code: int) -> float:
+    return float(_load().oracle_e4m3_value(int(code)))
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
 
 
 def select(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,
@@ -121,7 +152,8 @@ def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
            sel_idx: Optional[np.ndarray] = None, sel_cnt: Optional[np.ndarray] = None,
            scale: Optional[float] = None, per_q_head: bool = False) -> Tuple[np.ndarray, np.ndarray]:
     """Returns (out fp32 [B][Hq][D], lse fp32 [B][Hq]); dense when sel_idx is None.
-    With per_q_head, sel_idx has one row per query head."""
+    With per_q_head, sel_idx has one row per query head.  An fp8 cache attends
+    over its decoded e4m3 rows."""
     q = _c(q, np.uint16)
     page_table = _c(page_table, np.int32)
     seq_lens = _c(seq_lens, np.int32)
@@ -136,6 +168,14 @@ def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
         K = sel_idx.shape[2]
     out = np.empty((B, Hq, D), dtype=np.float32)
     lse = np.empty((B, Hq), dtype=np.float32)
+    if cache.fp8:
+        rc = _load().oracle_decode_fp8(_ptr(q), _ptr(cache.k8), _ptr(cache.v8), _ptr(cache.ks), _ptr(cache.vs),
+                                       _ptr(page_table), _ptr(seq_lens), B, Hq, cache.Hkv, D, cache.P, max_pages,
+                                       cache.n_phys, _ptr(sel_idx), _ptr(sel_cnt), K, int(bool(per_q_head)),
+                                       float(scale), _ptr(out), _ptr(lse))
+        if rc != 0:
+            raise ValueError(f"oracle_decode_fp8 failed ({rc})")
+        return out, lse
     rc = _load().oracle_decode_ex(_ptr(q), _ptr(cache.k), _ptr(cache.v), _ptr(page_table), _ptr(seq_lens),
                                   B, Hq, cache.Hkv, D, cache.P, max_pages, cache.n_phys, _ptr(sel_idx),
                                   _ptr(sel_cnt), K, int(bool(per_q_head)), float(scale), _ptr(out), _ptr(lse))
@@ -144,13 +184,14 @@ def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
     return out, lse
 
 
-def build_cache(wl, fill_bits: int) -> Cache:
+def build_cache(wl, fill_bits: int, fp8: bool = False, fill_code: int = 0, fill_scale: float = 0.0) -> Cache:
     """Pool + metadata after a workload's whole prefill, appended in 4096-token chunks.
 
     `wl` is a synthetic workload (token stream, slot mapping, pool size);
-    `fill_bits` is the bf16 pattern of pool slots that never receive a token."""
+    `fill_bits` is the bf16 pattern of pool slots that never receive a token
+    (`fill_code` / `fill_scale` for the e4m3 codes and scales of an fp8 pool)."""
     s = wl.spec
-    cache = Cache(wl.num_phys_pages, s.num_kv_heads, s.page_size, s.head_dim, fill_bits)
+    cache = Cache(wl.num_phys_pages, s.num_kv_heads, s.page_size, s.head_dim, fill_bits, fp8, fill_code, fill_scale)
     for a, b in wl.prefill_chunks():
         update_meta(cache, wl.k_tok[a:b], wl.v_tok[a:b], wl.slot_mapping[a:b])
     return cache

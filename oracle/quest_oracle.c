@@ -28,6 +28,14 @@
  *    above every other page, among themselves by lower page index, and they
  *    count toward the budget K.
  *
+ * FP8 pages (the pages name a quantized attention view but define no codec;
+ * the reading taken): every (token, kv head) row of K and of V is stored as
+ * 128 e4m3 codes and one fp32 scale s = amax(|row|) / 448; a value x is
+ * coded as e4m3(x / s), rounded to nearest with ties to even and saturated
+ * to +-448 (s = 0 and all codes 0 for an all-zero row); it decodes to
+ * e4m3_value(code) * s.  The page metadata stays the bf16 min / max of the
+ * keys as appended (before coding), so selection does not change.
+ *
  * It is written literally: the score uses the max-form above (not any
  * rearrangement of it), ranking is a full sort, attention is two passes
  * over an explicit score vector.  Accumulation is fp32 in the loop order
@@ -299,4 +307,137 @@ int oracle_decode(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_p
                   float* out, float* lse) {
     return oracle_decode_ex(q, k_pool, v_pool, page_table, seq_lens, B, Hq, Hkv, D, P, max_pages, n_phys,
                             sel_idx, sel_cnt, K, 0, scale, out, lse);
+}
+
+/* ---------------------------------------------------------------- FP8 (e4m3) pages
+ * e4m3: sign bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0
+ * holds the subnormals m * 2^-9; codes 0x7F / 0xFF are NaN; there are no
+ * infinities; the largest finite value is 0x7E = 448. */
+float oracle_e4m3_value(uint8_t c) {
+    const int sgn = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const float v = (e == 0) ? ldexpf((float)m, -9) : ldexpf((float)(8 + m), e - 10);
+    return sgn ? -v : v;
+}
+
+/* Nearest e4m3 value, ties to the even code, saturating to +-448; NaN -> 0x7F. */
+uint8_t oracle_e4m3_encode(float x) {
+    if (isnan(x)) return 0x7F;
+    const uint8_t sgn = signbit(x) ? 0x80 : 0x00;
+    float a = fabsf(x);
+    if (a >= 448.0f) return sgn | 0x7E;
+    if (a == 0.0f) return sgn;
+    /* Spacing of e4m3 values around a: 2^(E - 3) for a in [2^E, 2^(E+1)),
+     * E >= -6; 2^-9 below 2^-6 (subnormals). */
+    int E = ilogbf(a);
+    if (E < -6) E = -6;
+    const int qe = E - 3;
+    const float r = rintf(ldexpf(a, -qe));     /* integer multiple of the spacing; rintf rounds half to even */
+    const float v = ldexpf(r, qe);             /* exact e4m3 value (r = 16 carries into the next binade) */
+    if (v >= 448.0f) return sgn | 0x7E;
+    if (v == 0.0f) return sgn;
+    int ev = ilogbf(v);
+    if (ev < -6) return sgn | (uint8_t)ldexpf(v, 9);                 /* subnormal: m = v * 2^9 */
+    const int m = (int)ldexpf(v, 3 - ev) - 8;                         /* v = (8 + m) * 2^(ev - 3) */
+    return sgn | (uint8_t)(((ev + 7) << 3) | m);
+}
+
+/*
+ * Codes and scales of T appended tokens into FP8 pools at their slots:
+ *   k8, v8  [n_phys][Hkv][P][D] e4m3 codes;  ks, vs  [n_phys][Hkv][P] fp32 scales.
+ * (The bf16 rows and the metadata go through oracle_update_meta.)
+ */
+int oracle_quantize_rows(uint8_t* k8, uint8_t* v8, float* ks, float* vs,
+                         int64_t n_phys, int Hkv, int P, int D,
+                         const uint16_t* k_new, const uint16_t* v_new,
+                         const int32_t* slot_mapping, int64_t T) {
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t slot = slot_mapping[t];
+        int64_t page = slot / P;
+        int off = (int)(slot % P);
+        if (slot < 0 || page >= n_phys) return -2;
+        for (int h = 0; h < Hkv; ++h) {
+            for (int which = 0; which < 2; ++which) {
+                const uint16_t* src = (which ? v_new : k_new) + ((size_t)t * Hkv + h) * D;
+                uint8_t* dst = (which ? v8 : k8) + (((size_t)page * Hkv + h) * P + off) * D;
+                float* sc = (which ? vs : ks) + ((size_t)page * Hkv + h) * P + off;
+                float amax = 0.0f;
+                for (int i = 0; i < D; ++i) {
+                    float a = fabsf(bf16_bits_to_float(src[i]));
+                    if (a > amax) amax = a;
+                }
+                const float scale = amax / 448.0f;
+                *sc = scale;
+                for (int i = 0; i < D; ++i)
+                    dst[i] = scale > 0.0f ? oracle_e4m3_encode(bf16_bits_to_float(src[i]) / scale) : 0;
+            }
+        }
+    }
+    return 0;
+}
+
+/*
+ * oracle_decode over FP8 pages: key and value elements are
+ * e4m3_value(code) * scale of their row (fp32), otherwise as oracle_decode_ex.
+ */
+int oracle_decode_fp8(const uint16_t* q, const uint8_t* k8, const uint8_t* v8, const float* ks, const float* vs,
+                      const int32_t* page_table, const int32_t* seq_lens,
+                      int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
+                      const int32_t* sel_idx, const int32_t* sel_cnt, int K, int per_q_head, float scale,
+                      float* out, float* lse) {
+    if (Hq % Hkv != 0) return -1;
+    const int G = Hq / Hkv;
+    const int R = per_q_head ? Hq : Hkv;
+    float* z = (float*)malloc((size_t)max_pages * P * sizeof(float));
+    int64_t* tok_row = (int64_t*)malloc((size_t)max_pages * P * sizeof(int64_t));
+    if (!z || !tok_row) { free(z); free(tok_row); return -1; }
+    int rc = 0;
+    for (int b = 0; b < B && rc == 0; ++b) {
+        int len = seq_lens[b];
+        int n = (len + P - 1) / P;
+        if (n < 1 || n > max_pages) { rc = -2; break; }
+        for (int h = 0; h < Hq && rc == 0; ++h) {
+            int g = h / G;
+            int r = per_q_head ? h : g;
+            int count = sel_idx ? sel_cnt[(size_t)b * R + r] : n;
+            if (count < 0 || count > (sel_idx ? K : n)) { rc = -2; break; }
+            int ntok = 0;   /* attended tokens as row indices into [n_phys][Hkv][P] */
+            for (int j = 0; j < count; ++j) {
+                int p = sel_idx ? sel_idx[((size_t)b * R + r) * K + j] : j;
+                if (p < 0 || p >= n) { rc = -2; break; }
+                int64_t phys = page_table[(size_t)b * max_pages + p];
+                if (phys < 0 || phys >= n_phys) { rc = -2; break; }
+                int valid = (p == n - 1) ? len - P * (n - 1) : P;
+                for (int o = 0; o < valid; ++o) tok_row[ntok++] = (phys * Hkv + g) * P + o;
+            }
+            if (rc) break;
+            const uint16_t* qh = q + ((size_t)b * Hq + h) * D;
+            float* o_row = out + ((size_t)b * Hq + h) * D;
+            float m = -INFINITY;
+            for (int t = 0; t < ntok; ++t) {
+                const uint8_t* k = k8 + (size_t)tok_row[t] * D;
+                float dot = 0.0f;
+                for (int i = 0; i < D; ++i) dot += bf16_bits_to_float(qh[i]) * (oracle_e4m3_value(k[i]) * ks[tok_row[t]]);
+                z[t] = dot * scale;
+                if (z[t] > m) m = z[t];
+            }
+            float l = 0.0f;
+            for (int i = 0; i < D; ++i) o_row[i] = 0.0f;
+            for (int t = 0; t < ntok; ++t) {
+                float w = expf(z[t] - m);
+                l += w;
+                const uint8_t* v = v8 + (size_t)tok_row[t] * D;
+                for (int i = 0; i < D; ++i) o_row[i] += w * (oracle_e4m3_value(v[i]) * vs[tok_row[t]]);
+            }
+            if (ntok == 0) {
+                lse[(size_t)b * Hq + h] = -INFINITY;
+                continue;
+            }
+            for (int i = 0; i < D; ++i) o_row[i] /= l;
+            lse[(size_t)b * Hq + h] = m + logf(l);
+        }
+    }
+    free(z);
+    free(tok_row);
+    return rc;
 }

@@ -418,3 +418,75 @@ def test_per_q_head_decode_matches_sdpa_per_head():
     o2, l2 = oracle.decode(cache, wl.q, wl.page_table, wl.seq_lens, gsel, gcnt, scale=scale)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- FP8 (e4m3) pages
+
+def test_e4m3_codec_matches_torch_and_the_format():
+    """Encoding agrees with torch's float8_e4m3fn cast (round to nearest even)
+    on in-range values; decoding follows the format's definition; every
+    finite code round-trips; out-of-range values saturate to +-448."""
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 0.01,
+                         rng.standard_normal(2000) * 2.0 ** -8, [0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10,
+                                                                   1.0625, 1.1875, 3 * 2.0 ** -10, 440.0, 447.9]])
+    xs = xs.astype(np.float32)
+    want = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(x) for x in xs], dtype=np.uint8)
+    np.testing.assert_array_equal(got, want)
+    # decoding from the definition: sign, exponent bias 7, 3 mantissa bits, subnormals m * 2^-9
+    assert oracle.e4m3_value(0x38) == 1.0 and oracle.e4m3_value(0x7E) == 448.0
+    assert oracle.e4m3_value(0x01) == 2.0 ** -9 and oracle.e4m3_value(0x08) == 2.0 ** -6
+    assert oracle.e4m3_value(0xC5) == -3.25 and np.isnan(oracle.e4m3_value(0x7F))
+    finite = [c for c in range(256) if c & 0x7F != 0x7F]
+    vals = torch.tensor(finite, dtype=torch.uint8).view(torch.float8_e4m3fn).float().numpy()
+    for c, v in zip(finite, vals):
+        assert oracle.e4m3_value(c) == v
+        assert oracle.e4m3_encode(v) == c
+    for big in (448.5, 464.0, 500.0, 1e30):
+        assert oracle.e4m3_encode(big) == 0x7E and oracle.e4m3_encode(-big) == 0xFE
+    assert oracle.e4m3_encode(float("nan")) == 0x7F
+
+
+def test_fp8_rows_and_attention():
+    """Row scales are amax / 448 and the row's largest element codes to +-448;
+    every decoded element is within half an e4m3 spacing (x scale) of the
+    appended value; attention over an fp8 pool equals fp64 scaled-dot-product
+    attention over the decoded rows; the metadata is the bf16 pool's."""
+    spec = _tiny_spec(num_q_heads=4, num_kv_heads=2, ctx=70, seed=41, head_dim=8)
+    wl = synth.make_workload(spec)
+    c8 = oracle.build_cache(wl, synth.UNFILLED_BITS, fp8=True)
+    c16 = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    np.testing.assert_array_equal(c8.meta, c16.meta)
+    P = spec.page_size
+    dec = lambda codes: torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+    for t in range(wl.k_tok.shape[0]):
+        slot = int(wl.slot_mapping[t])
+        for h in range(spec.num_kv_heads):
+            for raw, codes, scales in ((wl.k_tok, c8.k8, c8.ks), (wl.v_tok, c8.v8, c8.vs)):
+                x = bf16_bits_to_f32(raw[t, h]).astype(np.float64)
+                s = float(scales[slot // P, h, slot % P])
+                amax = np.abs(x).max()
+                assert s == np.float32(np.float32(amax) / np.float32(448.0))
+                y = dec(codes[slot // P, h, slot % P]) * s
+                if amax > 0:
+                    assert np.abs(dec(codes[slot // P, h, slot % P])).max() == 448.0
+                spacing = 2.0 ** (np.maximum(np.floor(np.log2(np.maximum(np.abs(x) / s, 2.0 ** -6))), -6) - 3)
+                assert np.all(np.abs(y - x) <= 0.5 * spacing * s * (1 + 1e-6) + 1e-30)
+    sel, cnt, _ = oracle.select(c8, wl.q, wl.page_table, wl.seq_lens, 3)
+    out, lse = oracle.decode(c8, wl.q, wl.page_table, wl.seq_lens, sel, cnt, scale=0.3)
+    G = 2
+    qf = bf16_bits_to_f32(wl.q).astype(np.float64)
+    kd = dec(c8.k8) * c8.ks[..., None].astype(np.float64)
+    vd = dec(c8.v8) * c8.vs[..., None].astype(np.float64)
+    for b in range(spec.batch):
+        L = int(wl.seq_lens[b])
+        for h in range(4):
+            g = h // G
+            rows = [(int(wl.page_table[b, p]), o) for p in sel[b, g, : cnt[b, g]]
+                    for o in range(min(P, L - p * P))]
+            k = np.stack([kd[ph, g, o] for ph, o in rows])
+            v = np.stack([vd[ph, g, o] for ph, o in rows])
+            o_ref, l_ref = _sdpa_fp64(qf[b, h : h + 1], k, v, 0.3)
+            np.testing.assert_allclose(out[b, h], o_ref[0], rtol=2e-5, atol=2e-6)
+            np.testing.assert_allclose(lse[b, h], l_ref[0], rtol=2e-6, atol=2e-6)
