@@ -27,7 +27,7 @@
  *    8 query heads per kv head; query head h reads kv head h / (Hq / Hkv).
  *
  * Layouts (row-major, innermost last)
- *   k_pool, v_pool  bf16 [num_phys_pages][num_kv_heads][16][128]
+ *   k_pool, v_pool  bf16 [num_phys_pages][num_kv_heads][16][128]   (e4m3: see sv_cache)
  *   meta            bf16 [num_phys_pages][num_kv_heads][2][128]
  *                        [..][0][:] = per-channel key minimum of the page,
  *                        [..][1][:] = per-channel key maximum
@@ -64,15 +64,36 @@ enum sv_status {
 #define SV_DEVERR_SEQ_LEN    0x8u   /* seq_lens[b] < 1 or needs more than max_pages pages */
 #define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up waiting for its own bulk copies */
 
-/* The paged pool and its metadata: caller-owned device buffers. */
+/* K/V pool formats (sv_cache.kv_format). */
+#define SV_KV_BF16     0   /* k_pool, v_pool bf16 [pages][Hkv][16][128] */
+#define SV_KV_FP8_E4M3 1   /* k_pool, v_pool e4m3 bytes [pages][Hkv][16][128], one fp32 scale per row */
+
+/*
+ * The paged pool and its metadata: caller-owned device buffers.
+ *
+ * SV_KV_FP8_E4M3 (the pages name a quantized attention view but define no
+ * codec; the one used here): every (token, kv head) row of K and of V is 128
+ * e4m3 codes (sign, 4 exponent bits biased by 7, 3 mantissa bits, largest
+ * finite 448) and one fp32 scale s = max |x| / 448 over the row's bf16
+ * values; x is stored as e4m3(x / s), rounded to nearest with ties to even and
+ * saturated to +-448 (an all-zero row stores s = 0 and zero codes), and reads
+ * back as value(code) * s.  The metadata stays bf16 and holds the min / max
+ * of the keys as appended (before coding), so page selection is the same as
+ * for bf16 pools; only attention reads the coded rows.  All calls accept both
+ * formats except sv_quest_decode_step's single-launch kernel, which runs the
+ * separate kernels for fp8 pools.
+ */
 typedef struct sv_cache {
-    void* k_pool;             /* bf16 [num_phys_pages][num_kv_heads][16][128] */
-    void* v_pool;             /* bf16 [num_phys_pages][num_kv_heads][16][128] */
+    void* k_pool;             /* [num_phys_pages][num_kv_heads][16][128] of the format's element */
+    void* v_pool;
     void* meta;               /* bf16 [num_phys_pages][num_kv_heads][2][128]  */
     int64_t num_phys_pages;
     int32_t num_kv_heads;
     int32_t page_size;        /* must be 16 */
     int32_t head_dim;         /* must be 128 */
+    int32_t kv_format;        /* SV_KV_BF16 (zero) or SV_KV_FP8_E4M3 */
+    void* k_scale;            /* SV_KV_FP8_E4M3: fp32 [num_phys_pages][num_kv_heads][16]; else unused */
+    void* v_scale;
 } sv_cache;
 
 /*
@@ -252,11 +273,11 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
  *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
  *    with a call that may run at the same time; nothing in it needs to start
  *    at zero (the call clears its own counters first).
- *  - max_pages <= 8192 (131072 tokens) runs as one cooperative launch: every
- *    CTA co-resident, so the call returns SV_ERR_CUDA if the device cannot
- *    hold the grid (e.g. another context holds its SMs under MPS).  Larger
- *    max_pages runs sv_quest_select then sv_sparse_decode inside the same
- *    workspace.
+ *  - max_pages <= 8192 (131072 tokens) on a bf16 pool runs as one
+ *    cooperative launch: every CTA co-resident, so the call returns
+ *    SV_ERR_CUDA if the device cannot hold the grid (e.g. another context
+ *    holds its SMs under MPS).  Larger max_pages, and fp8 pools, run
+ *    sv_quest_select then sv_sparse_decode inside the same workspace.
  */
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
                          const int32_t* page_table, const int32_t* seq_lens, int32_t batch,

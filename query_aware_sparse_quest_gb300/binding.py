@@ -31,10 +31,14 @@ class sv_quest_opts(ctypes.Structure):
                 ("layer", ctypes.c_int32), ("dense_layers", ctypes.c_int32)]
 
 
+SV_KV_BF16, SV_KV_FP8_E4M3 = 0, 1
+
+
 class sv_cache(ctypes.Structure):
     _fields_ = [("k_pool", ctypes.c_void_p), ("v_pool", ctypes.c_void_p), ("meta", ctypes.c_void_p),
                 ("num_phys_pages", ctypes.c_int64), ("num_kv_heads", ctypes.c_int32),
-                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+                ("page_size", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("kv_format", ctypes.c_int32),
+                ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 def library_path() -> str:
@@ -104,12 +108,18 @@ def _check(fn: str, status: int) -> None:
 
 
 class Cache:
-    """A paged pool on the device: k/v bf16 [pages][Hkv][16][128], meta bf16 [pages][Hkv][2][128]."""
+    """A paged pool on the device: k/v [pages][Hkv][16][128] (bf16, or uint8 e4m3 codes with fp32 row
+    scales k_scale / v_scale [pages][Hkv][16]), meta bf16 [pages][Hkv][2][128]."""
 
-    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, meta: torch.Tensor):
+    def __init__(self, k_pool: torch.Tensor, v_pool: torch.Tensor, meta: torch.Tensor,
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None):
         self.k_pool, self.v_pool, self.meta = k_pool, v_pool, meta
+        self.k_scale, self.v_scale = k_scale, v_scale
         n, hkv, p, d = k_pool.shape
-        self.c = sv_cache(k_pool.data_ptr(), v_pool.data_ptr(), meta.data_ptr(), n, hkv, p, d)
+        fp8 = k_pool.dtype == torch.uint8
+        self.c = sv_cache(k_pool.data_ptr(), v_pool.data_ptr(), meta.data_ptr(), n, hkv, p, d,
+                          SV_KV_FP8_E4M3 if fp8 else SV_KV_BF16,
+                          k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None)
 
     @classmethod
     def empty(cls, num_phys_pages: int, num_kv_heads: int, device="cuda", page_size: int = 16,

@@ -23,6 +23,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
 int decode_max_splits(int pages);
 size_t decode_workspace_bytes(int batch, int num_q_heads, int splits);
 int read_error_step(uint32_t* flags, int reset);
+int read_error_decode_fp8(uint32_t* flags, int reset);
 int launch_step(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table, const int32_t* seq_lens,
                 int batch, int max_pages, int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, float softmax_scale,
                 void* out, float* lse, void* workspace, size_t ws_bytes, int sm_count, cudaStream_t stream);
@@ -57,6 +58,10 @@ int check_cache(const sv_cache* c) {
     if (c->num_phys_pages > INT_MAX) return SV_ERR_UNSUPPORTED;
     if (c->page_size != kPage || c->head_dim != kHeadDim) return SV_ERR_UNSUPPORTED;
     if (!aligned16(c->k_pool) || !aligned16(c->v_pool) || !aligned16(c->meta)) return SV_ERR_INVALID_ARG;
+    if (c->kv_format != SV_KV_BF16 && c->kv_format != SV_KV_FP8_E4M3) return SV_ERR_UNSUPPORTED;
+    if (c->kv_format == SV_KV_FP8_E4M3 && (!c->k_scale || !c->v_scale || !aligned16(c->k_scale) ||
+                                           !aligned16(c->v_scale)))
+        return SV_ERR_INVALID_ARG;
     return SV_OK;
 }
 
@@ -234,10 +239,13 @@ int sv_sparse_decode_ex(const sv_cache* cache, const void* q, int32_t num_q_head
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t max_pages, int32_t budget_pages) {
     if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_pages < 1 || budget_pages < 1) return 0;
-    if (max_pages <= kMaxStepPages)
-        return step_workspace_bytes(batch, num_q_heads, num_kv_heads, max_pages, budget_pages);
-    return scores_bytes(batch, num_kv_heads, max_pages) +
-           decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
+    // Enough for either path (the single launch, or the separate kernels that
+    // run for wider rows and fp8 pools).
+    const size_t separate = scores_bytes(batch, num_kv_heads, max_pages) +
+                            decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
+    if (max_pages > kMaxStepPages) return separate;
+    const size_t fused = step_workspace_bytes(batch, num_q_heads, num_kv_heads, max_pages, budget_pages);
+    return fused > separate ? fused : separate;
 }
 
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
@@ -259,10 +267,10 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (max_pages <= kMaxStepPages)
+    if (max_pages <= kMaxStepPages && cache->kv_format == SV_KV_BF16)
         return launch_step(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, sel_idx,
                            sel_cnt, softmax_scale, out, lse, workspace, workspace_bytes, sms, s);
-    // Two-stage path: scores at the front of the workspace, split-K partials after.
+    // Separate kernels: scores at the front of the workspace, split-K partials after.
     const size_t sb = scores_bytes(batch, cache->num_kv_heads, max_pages);
     float* scores = static_cast<float*>(workspace);
     if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s)))
@@ -281,6 +289,7 @@ int sv_get_device_error(uint32_t* flags, int reset) {
     if ((st = read_error_meta(flags, reset))) return st;
     if ((st = read_error_select(flags, reset))) return st;
     if ((st = read_error_step(flags, reset))) return st;
+    if ((st = read_error_decode_fp8(flags, reset))) return st;
     return read_error_decode(flags, reset);
 }
 

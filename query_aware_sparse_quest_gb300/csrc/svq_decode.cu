@@ -465,6 +465,12 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
 
 }  // namespace
 
+int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages, int sm_count, int max_splits);
+int launch_decode_fp8_split(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
+                            const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
+                            const int32_t* sel_cnt, int budget_pages, bool per_head, float softmax_scale, int splits,
+                            float* o_part, float2* ml_part, cudaStream_t stream);
+
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                   const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
@@ -478,11 +484,32 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
             return SV_ERR_CUDA;
         attr_set[dev] = true;
     }
+    const int pages = sel_idx ? budget_pages : max_pages;
+    if (c->kv_format == SV_KV_FP8_E4M3) {
+        const bool per_head8 = per_q_head && sel_idx;
+        const int rows8 = per_head8 ? num_q_heads : c->num_kv_heads;
+        const int splits8 = decode_fp8_splits(c, batch, rows8, pages, sm_count, decode_max_splits(pages));
+        if (splits8 < 1) return SV_ERR_CUDA;
+        if (decode_workspace_bytes(batch, num_q_heads, splits8) > workspace_bytes) return SV_ERR_WORKSPACE;
+        const size_t heads8 = static_cast<size_t>(batch) * num_q_heads * splits8;
+        float* o_part8 = static_cast<float*>(workspace);
+        float2* ml_part8 = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) +
+                                                     ((heads8 * kHeadDim * sizeof(float)) + 255) / 256 * 256);
+        int st = launch_decode_fp8_split(c, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
+                                         budget_pages, per_head8, softmax_scale, splits8, o_part8, ml_part8, stream);
+        if (st) return st;
+        const int64_t total_heads8 = static_cast<int64_t>(batch) * num_q_heads;
+        const int64_t blocks8 = (total_heads8 * 32 + kCombineThreads - 1) / kCombineThreads;
+        return launch_pdl(lse_combine_kernel, dim3(static_cast<unsigned>(blocks8)), dim3(kCombineThreads), 0, stream,
+                          static_cast<const float*>(o_part8), static_cast<const float2*>(ml_part8), splits8,
+                          total_heads8, static_cast<__nv_bfloat16*>(out), lse) == cudaSuccess
+                   ? SV_OK
+                   : SV_ERR_CUDA;
+    }
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flash_decode_split_kernel, kDecodeThreads,
                                                       kDecodeSmem) != cudaSuccess || per_sm < 1)
         return SV_ERR_CUDA;
-    const int pages = sel_idx ? budget_pages : max_pages;
     // Selection rows: one per kv head (its query heads share the page list),
     // or one per query head.  Dense decode always works per kv head.
     const bool per_head = per_q_head && sel_idx;

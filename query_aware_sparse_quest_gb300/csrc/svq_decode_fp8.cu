@@ -1,0 +1,466 @@
+// Split-K flash decode over FP8 (e4m3) K/V pages (sv_cache.kv_format =
+// SV_KV_FP8_E4M3): the same exact softmax attention over the selected pages
+// (SparseEngine page, "method key points": the AttentionView consumed by the
+// attention backend) with K and V rows stored as e4m3 codes and one fp32
+// scale per (token, kv head) row.
+//
+// Per CTA: one producer warp and four consumer warps over a 16-stage ring.  A
+// stage holds one page of one kv head: the K tile and the V tile, each a
+// 16 x 128-byte TMA box with the 128-byte swizzle (2 KB), plus the page's 16
+// K scales and 16 V scales (128 B, bulk copies) in a separate scale ring.
+// Producer lanes 2u and 2u+1 feed stage u (K, V): the pages whose list
+// position is u mod 16, each pair on its own.
+//
+// The tensor cores read the codes without a staging pass.  e4m3 values are
+// exact in f16, so codes convert to f16 pairs (cvt e4m3x2 -> f16x2) and feed
+// mma.sync m16n8k16 with f16 operands (q is converted once; P is f16):
+//  - K as the A operand of S^T = K Q^T: ldmatrix on the byte tile as 16-bit
+//    elements hands lane (g, q) four consecutive channels 4q .. 4q+3 of token
+//    rows g and g + 8 of a 16-channel block.  The MMA's k index is mapped to
+//    channels as (2q, 2q+1) -> (4q, 4q+1) and (2q+8, 2q+9) -> (4q+2, 4q+3); a
+//    dot product does not depend on the channel order, so the q fragments
+//    (B operand) use the same map.
+//  - V as the A operand of O^T += V^T P^T: ldmatrix.trans on the byte tile
+//    hands lane (g, q) channels 2g, 2g+1 of tokens 2q, 2q+1; byte permutes
+//    split them into an even-channel and an odd-channel fragment, i.e. two
+//    MMAs whose output rows are channels 2g (+16) and 2g+1 (+16) of the block.
+// Scales: the logit of token t is s_k(t) * (q . codes_t); the value weight of
+// token t is p_t * s_v(t) (the softmax sum uses p_t).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "svq_common.cuh"
+
+namespace svq {
+
+SVQ_DEFINE_ERROR_WORD(read_error_decode_fp8)
+
+constexpr int kF8Consumers = 4;
+constexpr int kF8Threads = (kF8Consumers + 1) * 32;
+constexpr int kF8Producer = kF8Consumers;
+constexpr int kF8Stages = 16;                    // pages in flight per CTA; lanes 2u, 2u+1 feed stage u
+constexpr int kF8Box = kPage * kHeadDim;         // 16 rows x 128 e4m3 = 2 KB
+constexpr int kF8Stage = 2 * kF8Box;             // K box | V box
+constexpr int kF8ScaleBytes = 2 * kPage * 4;     // 16 K scales | 16 V scales
+constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Stages * kF8ScaleBytes;
+static_assert(kF8Stages % kF8Consumers == 0, "each ring stage must belong to one consumer warp");
+static_assert(2 * kF8Stages == 32, "two producer lanes per stage");
+
+struct DecodeF8Args {
+    int64_t num_phys_pages;
+    int num_kv_heads;
+    const __nv_bfloat16* q;
+    int num_q_heads;
+    int group;                // query heads of one selection row
+    int rows_per_req;         // selection rows per request
+    int kv_div;               // row r reads kv head r / kv_div
+    const int32_t* page_table;
+    const int32_t* seq_lens;
+    int max_pages;
+    const int32_t* sel_idx;   // nullptr => dense
+    const int32_t* sel_cnt;
+    int K;
+    int num_splits;
+    float scale_log2;
+    const float* k_scale;     // [pages][Hkv][16]
+    const float* v_scale;
+    float* o_part;            // [B][Hq][S][128]
+    float2* ml_part;          // [B][Hq][S]
+};
+
+__device__ __forceinline__ float f8_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Two e4m3 codes (low byte first) -> f16x2 (exact).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+__device__ __forceinline__ uint32_t swz8(int row, int chunk) {
+    return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __grid_constant__ DecodeF8Args a,
+                                                                    const __grid_constant__ CUtensorMap tmap_k,
+                                                                    const __grid_constant__ CUtensorMap tmap_v) {
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ int s_valid[kF8Stages];
+    __shared__ __align__(8) uint64_t full_bar[kF8Stages];
+    __shared__ __align__(8) uint64_t empty_bar[kF8Stages];
+
+    const int split = blockIdx.x;
+    const int bg = blockIdx.y;
+    const int b = bg / a.rows_per_req;
+    const int g = bg % a.rows_per_req;
+    const int kvh = g / a.kv_div;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t raw_s = smem_addr(smem_raw);
+    const uint32_t ring_s = (raw_s + 1023u) & ~1023u;   // 128-byte swizzle wants 1024-byte aligned boxes
+    unsigned char* ring = smem_raw + (ring_s - raw_s);
+    const uint32_t scale_s = ring_s + kF8Stages * kF8Stage;
+    const float* scale_ring = reinterpret_cast<const float*>(ring + kF8Stages * kF8Stage);
+    const uint32_t full0 = smem_addr(&full_bar[0]);
+    const uint32_t empty0 = smem_addr(&empty_bar[0]);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kF8Stages; ++st) {
+            mbar_init(full0 + st * 8, 1);
+            mbar_init(empty0 + st * 8, 1);   // stage s is consumed by warp s % kF8Consumers alone
+        }
+        mbar_init_fence();
+    }
+    __syncthreads();
+
+    const int len = a.seq_lens[b];
+    int n = (len + kPage - 1) / kPage;
+    if (len < 1 || n > a.max_pages) {
+        if (threadIdx.x == 0 && split == 0) svq_flag(SV_DEVERR_SEQ_LEN);
+        n = len < 1 ? 0 : a.max_pages;
+    }
+
+    if (warp == kF8Producer) {
+        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_v);
+        const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
+        const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
+        pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
+        int count = n;
+        if (a.sel_idx) {
+            count = a.sel_cnt[bg];
+            if (count < 0 || count > a.K || count > n) {
+                if (lane == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
+                count = max(0, min(count, min(a.K, n)));
+            }
+        }
+        const int chunk = (count + a.num_splits - 1) / a.num_splits;
+        const int j0 = min(count, split * chunk);
+        const int my_count = min(count, j0 + chunk) - j0;
+        const int u = lane >> 1, part = lane & 1;   // stage u; part 0 moves K, part 1 moves V
+        const uint32_t fb = full0 + u * 8;
+        const uint32_t eb = empty0 + u * 8;
+        const void* tmap = part ? static_cast<const void*>(&tmap_v) : static_cast<const void*>(&tmap_k);
+        const float* scale_src = part ? a.v_scale : a.k_scale;
+        auto resolve = [&](int i, int& phys_out, int& valid_out) {
+            phys_out = -1;
+            valid_out = 0;
+            if (i < my_count) {
+                const int lp = sel_row ? sel_row[j0 + i] : j0 + i;
+                if (lp < 0 || lp >= n) {
+                    svq_flag(SV_DEVERR_SEL_IDX);
+                } else {
+                    const int ph = pt_row[lp];
+                    if (ph < 0 || ph >= a.num_phys_pages) {
+                        svq_flag(SV_DEVERR_PAGE_TABLE);
+                    } else {
+                        phys_out = ph;
+                        valid_out = (lp == n - 1) ? len - kPage * (n - 1) : kPage;
+                    }
+                }
+            }
+        };
+        int phys, valid;
+        resolve(u, phys, valid);
+        int last = -1;
+        bool ok = true;
+        for (int i = u; i < my_count; i += kF8Stages) {
+            int phys_next, valid_next;
+            resolve(i + kF8Stages, phys_next, valid_next);
+            if (i >= kF8Stages) ok = mbar_wait_bounded(eb, ((i / kF8Stages) - 1) & 1);
+            if (!ok) break;
+            if (part == 0) {
+                s_valid[u] = phys >= 0 ? valid : 0;
+                if (phys >= 0) mbar_arrive_expect_tx(fb, kF8Stage + kF8ScaleBytes);
+                else mbar_arrive(fb);
+            }
+            if (phys >= 0) {
+                const int64_t head_row = static_cast<int64_t>(phys) * a.num_kv_heads + kvh;
+                tma_load_2d(ring_s + u * kF8Stage + part * kF8Box, tmap, 0, static_cast<int>(head_row * kPage), fb);
+                bulk_copy_g2s(scale_s + u * kF8ScaleBytes + part * (kPage * 4), scale_src + head_row * kPage,
+                              kPage * 4, fb);
+            }
+            last = i;
+            phys = phys_next;
+            valid = valid_next;
+        }
+        if (!ok) svq_flag(SV_DEVERR_TIMEOUT);
+        // This lane's copies land before the CTA (and its shared memory) retires.
+        if (last >= 0) (void)mbar_wait_bounded(fb, (last / kF8Stages) & 1);
+        pdl_launch_dependents();
+        return;
+    }
+
+    // ---------------- consumer warps: warp w takes the split's pages w, w + 4, ...
+    const int quad = lane & 3;
+    const int row = lane >> 2;
+    // Q^T fragments (f16, B operand) for the 8 MMAs over 16-channel blocks
+    // c0 = 16 mm: k pair (2 quad, +1) -> channels c0 + 4 quad, +1; k pair
+    // (2 quad + 8, +9) -> channels c0 + 4 quad + 2, +3.
+    uint32_t qf[8][2];
+    {
+        const bool hv = row < a.group;
+        const __nv_bfloat16* qh =
+            a.q + (static_cast<int64_t>(b) * a.num_q_heads + g * a.group + (hv ? row : 0)) * kHeadDim;
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            const int c = 16 * mm + 4 * quad;
+            const uint2 w = hv ? *reinterpret_cast<const uint2*>(qh + c) : make_uint2(0u, 0u);
+            qf[mm][0] = pack_half2(bf16lo(w.x), bf16hi(w.x));
+            qf[mm][1] = pack_half2(bf16lo(w.y), bf16hi(w.y));
+        }
+    }
+    pdl_wait();
+    int count = n;
+    if (a.sel_idx) count = max(0, min(a.sel_cnt[bg], min(a.K, n)));
+    const int chunk = (count + a.num_splits - 1) / a.num_splits;
+    const int j0 = min(count, split * chunk);
+    const int my_count = min(count, j0 + chunk) - j0;
+
+    float o[8][4];   // o[2 cb + parity]: output channels 32 cb + 2 r + parity (+16 for rows r + 8)
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY};
+    float l_run[2] = {0.f, 0.f};
+    const int mat = lane >> 3, r8 = lane & 7;
+    const int krow = r8 + 8 * (mat & 1);        // K: matrices (rows 0-7 | 8-15) x (chunk 2kp | 2kp+1)
+    const int kchunk_off = mat >> 1;
+    const int vrow = r8 + 8 * (mat >> 1);       // V (trans): matrices (chunk 2cb | 2cb+1) x (tokens 0-7 | 8-15)
+    const int vchunk_off = mat & 1;
+    for (int i = warp; i < my_count; i += kF8Consumers) {
+        const int stage = i % kF8Stages;
+        const bool okw = mbar_wait_bounded(full0 + stage * 8, (i / kF8Stages) & 1);
+        if (__any_sync(0xffffffffu, !okw)) {
+            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
+            break;
+        }
+        const uint32_t st_s = ring_s + stage * kF8Stage;
+        const int valid = s_valid[stage];
+        if (valid < kPage) {
+            // Value rows past the fill hold whatever the pool holds there (NaN
+            // codes included): zero them.  Key rows are masked on the logits.
+            unsigned char* vb = ring + stage * kF8Stage + kF8Box;
+            for (int c = lane; c < (kPage - valid) * 8; c += 32) {
+                const int rr = valid + (c >> 3);
+                *reinterpret_cast<uint4*>(vb + swz8(rr, c & 7)) = make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+        }
+        const float* ks = scale_ring + stage * (kF8ScaleBytes / 4);
+        const float* vs = ks + kPage;
+
+        // S^T (16 tokens x 8 heads) = K Q^T over 128 channels.
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4(st_s + swz8(krow, 2 * kp + kchunk_off), r0, r1, r2, r3);
+            mma_f16_16816(sa, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                          e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
+            mma_f16_16816(sb, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                          e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+        }
+        const bool v0 = row < valid, v1 = row + 8 < valid;
+        const float ks0 = v0 ? ks[row] : 0.f, ks1 = v1 ? ks[row + 8] : 0.f;
+        const float x0 = v0 ? (sa[0] + sb[0]) * ks0 * a.scale_log2 : -INFINITY;   // token row,   head 2q
+        const float x1 = v0 ? (sa[1] + sb[1]) * ks0 * a.scale_log2 : -INFINITY;   // token row,   head 2q+1
+        const float x2 = v1 ? (sa[2] + sb[2]) * ks1 * a.scale_log2 : -INFINITY;   // token row+8, head 2q
+        const float x3 = v1 ? (sa[3] + sb[3]) * ks1 * a.scale_log2 : -INFINITY;   // token row+8, head 2q+1
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int s = 4; s < 32; s <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, s));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, s));
+        }
+        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+        const float alpha0 = f8_exp2(m_run[0] - base0), alpha1 = f8_exp2(m_run[1] - base1);
+        const float p0 = f8_exp2(x0 - base0), p1 = f8_exp2(x1 - base1);
+        const float p2 = f8_exp2(x2 - base0), p3 = f8_exp2(x3 - base1);
+        m_run[0] = mn0;
+        m_run[1] = mn1;
+        l_run[0] = l_run[0] * alpha0 + p0 + p2;
+        l_run[1] = l_run[1] * alpha1 + p1 + p3;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            o[mt][0] *= alpha0;
+            o[mt][1] *= alpha1;
+            o[mt][2] *= alpha0;
+            o[mt][3] *= alpha1;
+        }
+        // Value weights p_t * s_v(t) as P^T (tokens x heads, f16).
+        const float vs0 = v0 ? vs[row] : 0.f, vs1 = v1 ? vs[row + 8] : 0.f;
+        const uint32_t lo = pack_half2(p0 * vs0, p1 * vs0);   // token row:   heads 2q, 2q+1
+        const uint32_t hi = pack_half2(p2 * vs1, p3 * vs1);   // token row+8: heads 2q, 2q+1
+        const int src0 = (2 * quad) * 4 + (row >> 1);
+        const int src1 = (2 * quad + 1) * 4 + (row >> 1);
+        const uint32_t lo0 = __shfl_sync(0xffffffffu, lo, src0);
+        const uint32_t lo1 = __shfl_sync(0xffffffffu, lo, src1);
+        const uint32_t hi0 = __shfl_sync(0xffffffffu, hi, src0);
+        const uint32_t hi1 = __shfl_sync(0xffffffffu, hi, src1);
+        const uint32_t selector = (row & 1) ? 0x7632u : 0x5410u;
+        const uint32_t pb0 = __byte_perm(lo0, lo1, selector);
+        const uint32_t pb1 = __byte_perm(hi0, hi1, selector);
+
+        // O^T += V^T P^T, 32 channels per ldmatrix.trans: even and odd channels.
+#pragma unroll
+        for (int cb = 0; cb < 4; ++cb) {
+            uint32_t r0, r1, r2, r3;
+            ldmatrix_x4_trans(st_s + kF8Box + swz8(vrow, 2 * cb + vchunk_off), r0, r1, r2, r3);
+            mma_f16_16816(o[2 * cb], e4m3x2_to_f16x2(__byte_perm(r0, 0u, 0x0020u)),
+                          e4m3x2_to_f16x2(__byte_perm(r1, 0u, 0x0020u)), e4m3x2_to_f16x2(__byte_perm(r2, 0u, 0x0020u)),
+                          e4m3x2_to_f16x2(__byte_perm(r3, 0u, 0x0020u)), pb0, pb1);
+            mma_f16_16816(o[2 * cb + 1], e4m3x2_to_f16x2(__byte_perm(r0, 0u, 0x0031u)),
+                          e4m3x2_to_f16x2(__byte_perm(r1, 0u, 0x0031u)), e4m3x2_to_f16x2(__byte_perm(r2, 0u, 0x0031u)),
+                          e4m3x2_to_f16x2(__byte_perm(r3, 0u, 0x0031u)), pb0, pb1);
+        }
+        __syncwarp();   // every lane has read the stage before it is released
+        if (lane == 0) mbar_arrive(empty0 + stage * 8);
+    }
+
+#pragma unroll
+    for (int s = 4; s < 32; s <<= 1) {
+        l_run[0] += __shfl_xor_sync(0xffffffffu, l_run[0], s);
+        l_run[1] += __shfl_xor_sync(0xffffffffu, l_run[1], s);
+    }
+
+    // Merge the consumer warps through shared memory (every page of this CTA
+    // has been consumed, so no copy is in flight into the ring).
+    asm volatile("bar.sync 1, %0;" ::"n"(kF8Consumers * 32) : "memory");
+    float* sm_o = reinterpret_cast<float*>(ring);                   // [warp][8][128]
+    float* sm_m = sm_o + kF8Consumers * kMaxGroup * kHeadDim;       // [warp][8]
+    float* sm_l = sm_m + kF8Consumers * kMaxGroup;                  // [warp][8]
+    {
+        float* ow = sm_o + warp * kMaxGroup * kHeadDim;
+        const int h0 = 2 * quad, h1 = 2 * quad + 1;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            const int ch = 32 * (mt >> 1) + 2 * row + (mt & 1);
+            ow[h0 * kHeadDim + ch] = o[mt][0];
+            ow[h1 * kHeadDim + ch] = o[mt][1];
+            ow[h0 * kHeadDim + ch + 16] = o[mt][2];
+            ow[h1 * kHeadDim + ch + 16] = o[mt][3];
+        }
+        if (row == 0) {
+            sm_m[warp * kMaxGroup + h0] = m_run[0];
+            sm_m[warp * kMaxGroup + h1] = m_run[1];
+            sm_l[warp * kMaxGroup + h0] = l_run[0];
+            sm_l[warp * kMaxGroup + h1] = l_run[1];
+        }
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kF8Consumers * 32) : "memory");
+    const int S = a.num_splits;
+    const int64_t qbase = static_cast<int64_t>(b) * a.num_q_heads + g * a.group;
+    for (int idx = threadIdx.x; idx < a.group * kHeadDim; idx += kF8Consumers * 32) {
+        const int h = idx / kHeadDim, d = idx % kHeadDim;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kF8Consumers; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + h]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kF8Consumers; ++w) {
+                const float e = f8_exp2(sm_m[w * kMaxGroup + h] - M);
+                L += sm_l[w * kMaxGroup + h] * e;
+                O += sm_o[(w * kMaxGroup + h) * kHeadDim + d] * e;
+            }
+        }
+        a.o_part[((qbase + h) * S + split) * kHeadDim + d] = O;
+        if (d == 0) a.ml_part[(qbase + h) * S + split] = make_float2(M, L);
+    }
+}
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 f8_tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// An e4m3 pool [pages][kv heads][16][128] as a 2-D byte tensor
+// [pages * kv heads * 16 rows][128], read in 16 x 128-byte boxes with the
+// 128-byte swizzle.
+bool encode_f8_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = f8_tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kPage)};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(pool), dims, strides, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages, int sm_count, int max_splits) {
+    static bool attr_set[64] = {};
+    const int dev = current_device();
+    if (dev < 0) return -1;
+    if (dev >= 64 || !attr_set[dev]) {
+        if (cudaFuncSetAttribute(flash_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem) !=
+            cudaSuccess)
+            return -1;
+        if (dev < 64) attr_set[dev] = true;
+    }
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flash_decode_fp8_kernel, kF8Threads, kF8Smem) !=
+            cudaSuccess ||
+        per_sm < 1)
+        return -1;
+    (void)c;
+    (void)pages;
+    const int bh = batch * rows_per_req;
+    const int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm) / bh);
+    return max(1, min(splits, max_splits));
+}
+
+int launch_decode_fp8_split(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
+                            const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
+                            const int32_t* sel_cnt, int budget_pages, bool per_head, float softmax_scale, int splits,
+                            float* o_part, float2* ml_part, cudaStream_t stream) {
+    const int64_t rows = c->num_phys_pages * c->num_kv_heads * kPage;
+    if (rows > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
+    CUtensorMap tmap_k, tmap_v;
+    if (!encode_f8_pool_map(&tmap_k, c->k_pool, rows) || !encode_f8_pool_map(&tmap_v, c->v_pool, rows))
+        return SV_ERR_CUDA;
+    DecodeF8Args a;
+    a.num_phys_pages = c->num_phys_pages;
+    a.num_kv_heads = c->num_kv_heads;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.num_q_heads = num_q_heads;
+    a.group = per_head ? 1 : num_q_heads / c->num_kv_heads;
+    a.rows_per_req = per_head ? num_q_heads : c->num_kv_heads;
+    a.kv_div = per_head ? num_q_heads / c->num_kv_heads : 1;
+    a.page_table = page_table;
+    a.seq_lens = seq_lens;
+    a.max_pages = max_pages;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.K = sel_idx ? budget_pages : 0;
+    a.num_splits = splits;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.k_scale = static_cast<const float*>(c->k_scale);
+    a.v_scale = static_cast<const float*>(c->v_scale);
+    a.o_part = o_part;
+    a.ml_part = ml_part;
+    const int bh = batch * a.rows_per_req;
+    return launch_pdl(flash_decode_fp8_kernel, dim3(splits, bh), dim3(kF8Threads), kF8Smem, stream, a, tmap_k,
+                      tmap_v) == cudaSuccess
+               ? SV_OK
+               : SV_ERR_CUDA;
+}
+
+}  // namespace svq

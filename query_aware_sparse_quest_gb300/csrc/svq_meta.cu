@@ -8,13 +8,18 @@ namespace svq {
 SVQ_DEFINE_ERROR_WORD(read_error_meta)
 
 // One warp per (token t, kv head h).  Lanes 0-15 copy the key row, lanes
-// 16-31 the value row, 16 bytes each.  The warp of the last token of a run
+// 16-31 the value row, 16 bytes (8 values) each.  FP8 pools: each half-warp
+// takes the row's max |x| (4 shuffles), stores the fp32 scale s = max / 448
+// and the row's codes e4m3(x / s) (IEEE division, round to nearest even,
+// saturating), 8 bytes per lane.  The warp of the last token of a run
 // of consecutive tokens bound for one page also rebuilds that page's
 // metadata for head h: lane l < 16 produces kmin of channels 8l..8l+7, lane
 // l >= 16 kmax of channels 8(l-16)..; the run's first offset decides whether
 // the stored min/max are kept (offset > 0) or restarted (offset 0).
+template <bool FP8>
 __global__ void __launch_bounds__(256) append_kv_meta_kernel(
-    __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ v_pool, __nv_bfloat16* __restrict__ meta,
+    void* __restrict__ k_pool, void* __restrict__ v_pool, __nv_bfloat16* __restrict__ meta,
+    float* __restrict__ k_scale, float* __restrict__ v_scale,
     int64_t num_phys_pages, int num_kv_heads, const __nv_bfloat16* __restrict__ k_new,
     const __nv_bfloat16* __restrict__ v_new, const int32_t* __restrict__ slot_mapping, int64_t num_tokens) {
     const int lane = threadIdx.x & 31;
@@ -33,12 +38,40 @@ __global__ void __launch_bounds__(256) append_kv_meta_kernel(
     const int off = slot % kPage;
     const int chunk = lane & 15;
 
-    // Row copy.
+    // Row copy (bf16) or row coding (fp8).
     {
         const __nv_bfloat16* src = (lane < 16 ? k_new : v_new) + (t * num_kv_heads + h) * kHeadDim + chunk * 8;
-        __nv_bfloat16* dst = (lane < 16 ? k_pool : v_pool) +
-                             ((page * num_kv_heads + h) * kPage + off) * kHeadDim + chunk * 8;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        const int64_t row = (page * num_kv_heads + h) * kPage + off;
+        const uint4 w = *reinterpret_cast<const uint4*>(src);
+        if (!FP8) {
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(lane < 16 ? k_pool : v_pool) + row * kHeadDim + chunk * 8;
+            *reinterpret_cast<uint4*>(dst) = w;
+        } else {
+            const uint32_t x[4] = {w.x, w.y, w.z, w.w};
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                f[2 * e] = bf16lo(x[e]);
+                f[2 * e + 1] = bf16hi(x[e]);
+            }
+            float amax = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float sc = __fdiv_rn(amax, 448.f);
+            uint32_t packed[2] = {0u, 0u};
+            if (sc > 0.f) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const uint32_t code = __nv_cvt_float_to_fp8(__fdiv_rn(f[e], sc), __NV_SATFINITE, __NV_E4M3);
+                    packed[e >> 2] |= code << (8 * (e & 3));
+                }
+            }
+            unsigned char* dst = static_cast<unsigned char*>(lane < 16 ? k_pool : v_pool) + row * kHeadDim + chunk * 8;
+            *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+            if (chunk == 0) (lane < 16 ? k_scale : v_scale)[row] = sc;
+        }
     }
 
     // Is t the last token of its page's run in this call?
@@ -85,11 +118,17 @@ int launch_update_meta(const sv_cache* c, const void* k_new, const void* v_new, 
     const int64_t items = num_tokens * c->num_kv_heads;
     const int64_t blocks = (items * 32 + 255) / 256;
     if (blocks > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
-    append_kv_meta_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<__nv_bfloat16*>(c->k_pool), static_cast<__nv_bfloat16*>(c->v_pool),
-        static_cast<__nv_bfloat16*>(c->meta), c->num_phys_pages, c->num_kv_heads,
-        static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new), slot_mapping,
-        num_tokens);
+    const auto kn = static_cast<const __nv_bfloat16*>(k_new);
+    const auto vn = static_cast<const __nv_bfloat16*>(v_new);
+    auto* meta = static_cast<__nv_bfloat16*>(c->meta);
+    if (c->kv_format == SV_KV_FP8_E4M3)
+        append_kv_meta_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            c->k_pool, c->v_pool, meta, static_cast<float*>(c->k_scale), static_cast<float*>(c->v_scale),
+            c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping, num_tokens);
+    else
+        append_kv_meta_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+            c->k_pool, c->v_pool, meta, nullptr, nullptr, c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping,
+            num_tokens);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

@@ -34,15 +34,24 @@ class DeviceWorkload:
 
 
 def upload(wl: Workload, device="cuda", prefill: bool = True, chunk_tokens: int = 4096,
-           fill_bits: int = UNFILLED_BITS) -> DeviceWorkload:
-    """Allocates the pool (unfilled slots hold the bf16 pattern `fill_bits`),
+           fill_bits: int = UNFILLED_BITS, fp8: bool = False, fill_code: int = 0x7F,
+           fill_scale: float = float("nan")) -> DeviceWorkload:
+    """Allocates the pool (unfilled slots hold the bf16 pattern `fill_bits`;
+    for an fp8 pool the e4m3 code `fill_code` and the scale `fill_scale`),
     copies q / page table / lengths, and appends the prefill stream."""
     s = wl.spec
     shape = (wl.num_phys_pages, s.num_kv_heads, s.page_size, s.head_dim)
-    k = torch.full(shape, int(np.int16(np.uint16(fill_bits))), dtype=torch.int16, device=device).view(torch.bfloat16)
-    v = k.clone()
     meta = torch.zeros((wl.num_phys_pages, s.num_kv_heads, 2, s.head_dim), dtype=torch.bfloat16, device=device)
-    cache = binding.Cache(k, v, meta)
+    if fp8:
+        k = torch.full(shape, int(fill_code), dtype=torch.uint8, device=device)
+        v = k.clone()
+        ks = torch.full(shape[:3], float(fill_scale), dtype=torch.float32, device=device)
+        vs = ks.clone()
+        cache = binding.Cache(k, v, meta, ks, vs)
+    else:
+        k = torch.full(shape, int(np.int16(np.uint16(fill_bits))), dtype=torch.int16, device=device).view(torch.bfloat16)
+        v = k.clone()
+        cache = binding.Cache(k, v, meta)
     dw = DeviceWorkload(wl=wl, cache=cache, q=bf16_tensor(wl.q, device),
                         page_table=torch.from_numpy(wl.page_table).to(device),
                         seq_lens=torch.from_numpy(wl.seq_lens).to(device))

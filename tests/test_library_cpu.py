@@ -193,3 +193,17 @@ def test_select_ex_and_decode_ex_option_checks(lib):
     assert need == 8 * 32 * 100 * 4
     assert sel(binding.quest_opts(per_q_head=True), ws_bytes=need - 1) == SV_ERR_WORKSPACE
     assert binding.sv_quest_select_ex_workspace_size(8, 32, 4, 100, None) == 8 * 4 * 100 * 4
+
+
+def test_fp8_cache_checks(lib):
+    def cache(fmt, ks=0x10000, vs=0x10000):
+        c = _fake_cache()
+        c.kv_format, c.k_scale, c.v_scale = fmt, ks, vs
+        return ctypes.byref(c)
+
+    def sel(c):
+        return lib.sv_quest_select(c, FAKE, 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, FAKE, 1 << 30, None)
+    assert sel(cache(binding.SV_KV_FP8_E4M3, ks=0)) == SV_ERR_INVALID_ARG      # scales required
+    assert sel(cache(binding.SV_KV_FP8_E4M3, vs=0x10004)) == SV_ERR_INVALID_ARG  # 16-byte aligned
+    assert sel(cache(7)) == SV_ERR_UNSUPPORTED
+    assert ctypes.sizeof(binding.sv_cache) == 64
