@@ -139,7 +139,10 @@ def algorithmic_bytes(wl):
     sel_rd = int(sel.sum()) * Hkv * 4 * 2          # sel_idx + page-table entry per selected page
     out = s.batch * Hq * D * 2 + s.batch * Hq * 4
     dense_kv = int(n.sum()) * Hkv * P * D * 2 * 2
+    kv8 = int(sel.sum()) * Hkv * P * (D + 4) * 2      # e4m3 rows + fp32 row scales, K and V
     return {
+        "fp8_step": meta + kv8 + pt + q + out,
+        "fp8_decode": kv8 + sel_rd + q,
         "step": meta + kv + pt + q + out,
         "score_pages_kernel": meta + pt + q + scores_w,
         "flash_decode_split_kernel": kv + sel_rd + q,
@@ -313,6 +316,26 @@ def run_gpu(args):
         binding.sv_quest_update_meta(dw.cache, k_new, v_new, slots)
 
     append_ms = float(np.mean(timed(append, max(3, min(args.steps, 200)))))
+
+    # ---- the same step over an fp8 (e4m3) pool of the same tokens
+    dw8 = resident.upload(wl, device=dev, fp8=True)
+    sel8, cnt8 = resident.select_buffers(B, Hkv, K, dev)
+    out8, lse8 = torch.empty_like(out), torch.empty_like(lse)
+
+    def step8():
+        binding.sv_quest_score(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, scores)
+        binding.sv_quest_topk(scores, dw8.seq_lens, K, sel8, cnt8)
+        binding.sv_sparse_decode(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, sel8, cnt8, out8, lse8, ws)
+
+    for _ in range(3):
+        step8()
+    g_step8 = capture(step8)
+    fp8_ms = float(np.mean(timed(g_step8.replay, max(3, min(args.steps, 200)))))
+    fp8_dec_ms = float(np.mean(timed(
+        lambda: binding.sv_sparse_decode(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, sel8, cnt8, out8, lse8, ws),
+        max(3, min(args.steps, 200)))))
+    fp8_same_sel = bool(torch.equal(cnt8, sel_cnt))
+    del dw8
     pages_touched = -(-T // spec.page_size)
     append_bytes = (2 * T * Hkv * D * 2            # k_new, v_new read
                     + 2 * T * Hkv * D * 2          # pool rows written
@@ -389,6 +412,12 @@ def run_gpu(args):
         "fused_step": {"ms_per_step": round(fused_ms, 5), "steps_per_s": round(1e3 / fused_ms, 2),
                        "agrees_with_step": fused_agree,
                        "note": "sv_quest_decode_step: the same step as one cooperative launch, timed alone"},
+        "fp8_step": {"ms_per_step": round(fp8_ms, 5), "steps_per_s": round(1e3 / fp8_ms, 2),
+                     "bytes": ab["fp8_step"], "gbs": round(ab["fp8_step"] / (fp8_ms * 1e-3) / 1e9, 1),
+                     "sparse_decode_ms": round(fp8_dec_ms, 5),
+                     "decode_gbs": round(ab["fp8_decode"] / (fp8_dec_ms * 1e-3) / 1e9, 1),
+                     "same_selection_counts": fp8_same_sel,
+                     "note": "same step over an e4m3 K/V pool with per-row fp32 scales (bf16 metadata)"},
         "prefill_append": {"tokens": T, "ms": round(append_ms, 5), "bytes": append_bytes,
                            "gbs": round(append_bytes / (append_ms * 1e-3) / 1e9, 1)},
         "gpu_launches": launches_per_step * args.steps,

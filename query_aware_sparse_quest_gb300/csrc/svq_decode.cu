@@ -29,6 +29,9 @@ constexpr int kBoxBytes = kPage * 64 * 2;         // one TMA box: 16 rows x 64 c
 constexpr int kStageBytes = 4 * kBoxBytes;        // K lo | K hi | V lo | V hi
 constexpr int kDecodeSmem = kStages * kStageBytes + 1024;   // + slack for 1024-byte alignment
 constexpr int kMaxSplits = 64;
+#ifndef SVQ_DECODE_WAVE_PERMILLE
+#define SVQ_DECODE_WAVE_PERMILLE 1000   // split CTAs as a fraction of one full wave
+#endif
 constexpr int kMinPagesPerSplit = 8;
 
 struct DecodeArgs {
@@ -367,9 +370,10 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
 }
 
 // One warp per (request, query head); lane l owns channels 4l .. 4l+3.
-// Split statistics are read one split per lane; partial outputs are loaded
-// eight splits at a time before they are combined.
+// The split statistics (one split per lane) and the first 16 splits' partial
+// outputs are requested together, so the common case costs one round trip.
 constexpr int kCombineThreads = 128;
+constexpr int kCombineBatch = 16;
 
 __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(const float* __restrict__ o_part,
                                                                       const float2* __restrict__ ml_part,
@@ -381,8 +385,18 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(const floa
     pdl_wait();   // partials come from the split kernel launched just before
     if (qh >= total_heads) return;
     const float2* ml = ml_part + qh * num_splits;
+    const float* ob = o_part + qh * num_splits * kHeadDim + 4 * lane;
     const float2 v0 = lane < num_splits ? ml[lane] : make_float2(-INFINITY, 0.f);
     const float2 v1 = lane + 32 < num_splits ? ml[lane + 32] : make_float2(-INFINITY, 0.f);
+    // The first kCombineBatch splits' partials go to shared memory with async
+    // copies issued back to back, so they arrive in the round trip of the
+    // statistics above.
+    __shared__ __align__(16) float4 stash[kCombineThreads / 32][kCombineBatch][32];
+    float4* mine = &stash[threadIdx.x >> 5][0][lane];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u)
+        cp_async16(smem_addr(mine + u * 32), ob + u * kHeadDim, u < num_splits ? 16u : 0u);
+    cp_async_commit();
     float M = fmaxf(v0.x, v1.x);
 #pragma unroll
     for (int s = 16; s >= 1; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
@@ -393,24 +407,27 @@ __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(const floa
     for (int s = 16; s >= 1; s >>= 1) L += __shfl_xor_sync(0xffffffffu, L, s);
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const float* ob = o_part + qh * num_splits * kHeadDim + 4 * lane;
-    for (int s0 = 0; s0 < num_splits; s0 += 8) {
-        float4 p[8];
+    auto add = [&](const float4& x, int s) {
+        const float e = __shfl_sync(0xffffffffu, s < 32 ? e0 : e1, s & 31);
+        if (s < num_splits) {
+            acc.x += x.x * e;
+            acc.y += x.y * e;
+            acc.z += x.z * e;
+            acc.w += x.w * e;
+        }
+    };
+    cp_async_wait<0>();
+    __syncwarp();
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) add(mine[u * 32], u);
+    for (int s0 = kCombineBatch; s0 < num_splits; s0 += 8) {
+        float4 r[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-            p[u] = s0 + u < num_splits ? *reinterpret_cast<const float4*>(ob + (s0 + u) * kHeadDim)
+            r[u] = s0 + u < num_splits ? *reinterpret_cast<const float4*>(ob + (s0 + u) * kHeadDim)
                                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int s = s0 + u;
-            const float e = __shfl_sync(0xffffffffu, s < 32 ? e0 : e1, s & 31);
-            if (s < num_splits) {
-                acc.x += p[u].x * e;
-                acc.y += p[u].y * e;
-                acc.z += p[u].z * e;
-                acc.w += p[u].w * e;
-            }
-        }
+        for (int u = 0; u < 8; ++u) add(r[u], s0 + u);
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     __nv_bfloat162 r01 = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
@@ -515,7 +532,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     const bool per_head = per_q_head && sel_idx;
     const int rows_per_req = per_head ? num_q_heads : c->num_kv_heads;
     const int bh = batch * rows_per_req;
-    int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm) / bh);
+    int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm * SVQ_DECODE_WAVE_PERMILLE / 1000) / bh);
     splits = max(1, min(splits, decode_max_splits(pages)));
     if (decode_workspace_bytes(batch, num_q_heads, splits) > workspace_bytes) return SV_ERR_WORKSPACE;
 

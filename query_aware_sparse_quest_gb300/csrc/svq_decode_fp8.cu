@@ -423,7 +423,10 @@ int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages,
     (void)c;
     (void)pages;
     const int bh = batch * rows_per_req;
-    const int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm) / bh);
+#ifndef SVQ_DECODE_WAVE_PERMILLE
+#define SVQ_DECODE_WAVE_PERMILLE 1000   // split CTAs as a fraction of one full wave
+#endif
+    const int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm * SVQ_DECODE_WAVE_PERMILLE / 1000) / bh);
     return max(1, min(splits, max_splits));
 }
 
