@@ -123,8 +123,18 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
         pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
         int count = n;
+        int spec_lp = -1;        // this lane's first list entry, fetched with the count
+        bool spec_ok = false;    // true when the count is the one guessed below
         if (a.sel_idx) {
+            // The top-K writes min(K, n) entries; guess that count so that the
+            // first list entries load in the same round trip as the count.
+            const int guess = min(a.K, n);
+            const int chunk_g = (guess + a.num_splits - 1) / a.num_splits;
+            const int j0_g = min(guess, split * chunk_g);
+            const int my_g = min(guess, j0_g + chunk_g) - j0_g;
+            spec_lp = lane < my_g ? sel_row[j0_g + lane] : -1;
             count = a.sel_cnt[bg];
+            spec_ok = count == guess;
             if (count < 0 || count > a.K || count > n) {
                 if (lane == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
                 count = max(0, min(count, min(a.K, n)));
@@ -145,7 +155,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
             phys_out = -1;
             valid_out = 0;
             if (ii < my_count) {
-                const int lp = sel_row ? sel_row[j0 + ii] : j0 + ii;
+                const int lp = sel_row ? (base == 0 && spec_ok ? spec_lp : sel_row[j0 + ii]) : j0 + ii;
                 if (lp < 0 || lp >= n) {
                     svq_flag(SV_DEVERR_SEL_IDX);
                 } else {
