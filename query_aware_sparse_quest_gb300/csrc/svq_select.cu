@@ -96,27 +96,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         }
         mbar_init_fence();
     }
-    // Stage this request's query (Hq x 128 bf16, at most 16 KB) in shared
-    // memory with 16-byte loads, then fold each kv group's query heads into
-    // Qp / Qn.  q is an input of the step, so this overlaps the previous kernel.
-    const int hq = HKV * group;
-    {
-        const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
-        uint4* qdst = reinterpret_cast<uint4*>(qstage);
-        for (int i = threadIdx.x; i < hq * kHeadDim / 8; i += kScoreThreads) qdst[i] = qsrc[i];
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < HKV * kHeadDim; idx += kScoreThreads) {
-        const int j = idx / kHeadDim, ch = idx % kHeadDim;
-        float qp = 0.f, qn = 0.f;
-        for (int h = 0; h < group; ++h) {
-            const float v = __bfloat162float(qstage[(j * group + h) * kHeadDim + ch]);
-            qp += fmaxf(v, 0.f);
-            qn += fminf(v, 0.f);
-        }
-        coef[j][0][ch] = qn;
-        coef[j][1][ch] = qp;
-    }
     __syncthreads();
 
     const int len = seq_lens[b];
@@ -127,6 +106,33 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     }
     const int cta_begin = blockIdx.x * pages_per_cta;
     const int span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
+
+    if (warp != kScoreProducer) {
+        // Consumers stage this request's query (Hq x 128 bf16, at most 16 KB)
+        // in shared memory with 16-byte loads and fold each kv group's query
+        // heads into Qp / Qn, while the producer already streams metadata.
+        // q is an input of the step, so this also overlaps the previous kernel.
+        constexpr int kConsumerThreads = kScoreConsumers * 32;
+        const int hq = HKV * group;
+        {
+            const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
+            uint4* qdst = reinterpret_cast<uint4*>(qstage);
+            for (int i = threadIdx.x; i < hq * kHeadDim / 8; i += kConsumerThreads) qdst[i] = qsrc[i];
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+        for (int idx = threadIdx.x; idx < HKV * kHeadDim; idx += kConsumerThreads) {
+            const int j = idx / kHeadDim, ch = idx % kHeadDim;
+            float qp = 0.f, qn = 0.f;
+            for (int h = 0; h < group; ++h) {
+                const float v = __bfloat162float(qstage[(j * group + h) * kHeadDim + ch]);
+                qp += fmaxf(v, 0.f);
+                qn += fminf(v, 0.f);
+            }
+            coef[j][0][ch] = qn;
+            coef[j][1][ch] = qp;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
+    }
     // Metadata may come from an append launched just before, and the previous
     // step's top-K may still read the score buffer.
     pdl_wait();
