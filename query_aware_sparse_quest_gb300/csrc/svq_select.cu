@@ -133,17 +133,19 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
     }
+    // The page table, like q and the lengths, is an input of the step: the
+    // producer's first entries load before the wait below.
+    const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
+    int nxt = (warp == kScoreProducer && lane < span) ? pt_row[lane] : 0;
     // Metadata may come from an append launched just before, and the previous
     // step's top-K may still read the score buffer.
     pdl_wait();
 
     if (warp == kScoreProducer) {
-        const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
         const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(meta);
         const uint32_t ring_s = smem_addr(ring);
         int issued_last = -1;   // highest page this lane issued
         bool failed = false;
-        int nxt = lane < span ? pt_row[lane] : 0;
         for (int p = lane; p < span; p += 32) {
             const int phys = nxt;
             if (p + 32 < span) nxt = pt_row[p + 32];
