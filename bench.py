@@ -13,9 +13,10 @@ replayed.  Inputs are resident in HBM; L2 is flushed before every timed step;
 each step is bracketed by CUDA events on the launching stream, all K steps
 are enqueued before one synchronisation, and the K step times are summed.
 Per-kernel durations come from a second pass that times each call alone.
-The end-to-end figure goes through the public calls (sv_quest_select +
-sv_sparse_decode) with q, page table and lengths copied in from pinned host
-memory and out / lse copied back inside the timed region.
+The end-to-end figure goes through the public one-call step
+(sv_quest_decode_step: the same four kernels) with q, page table and lengths
+copied in from pinned host memory and out / lse copied back inside the timed
+region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -168,10 +169,11 @@ def algorithmic_bytes(wl):
 
 # Kernels each public call launches (include/svquest.h): sv_quest_score and
 # sv_quest_topk one each, sv_sparse_decode two (split-K flash decode, then the
-# log-sum-exp combine), sv_quest_decode_step one cooperative kernel (after a
-# memset of its counters), sv_quest_update_meta one.
-KERNELS_PER_CALL = {"sv_quest_score": 1, "sv_quest_topk": 1, "sv_sparse_decode": 2,
-                    "sv_quest_decode_step": 1, "sv_quest_update_meta": 1}
+# log-sum-exp combine), sv_quest_decode_step the same four, the single-launch
+# step one cooperative kernel (after a memset of its counters),
+# sv_quest_update_meta one.
+KERNELS_PER_CALL = {"sv_quest_score": 1, "sv_quest_topk": 1, "sv_sparse_decode": 2, "sv_quest_decode_step": 4,
+                    "sv_quest_decode_step_single_launch": 1, "sv_quest_update_meta": 1}
 STEP_CALLS = ("sv_quest_score", "sv_quest_topk", "sv_sparse_decode")
 
 
@@ -303,13 +305,14 @@ def run_gpu(args):
     # ---- dense (all pages) comparator
     dense_ms = float(np.mean(timed(g_dense.replay, max(3, min(args.steps, 50)))))
 
-    # ---- the same step as one cooperative launch (sv_quest_decode_step)
+    # ---- the same step as one cooperative launch (sv_quest_decode_step_single_launch)
     sel2, cnt2 = resident.select_buffers(B, Hkv, K, dev)
     out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
     ws_step = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, max_pages, K), dev)
 
     def fused():
-        binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel2, cnt2, out2, lse2, ws_step)
+        binding.sv_quest_decode_step_single_launch(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel2, cnt2, out2,
+                                                   lse2, ws_step)
 
     fused()
     step()   # the three-call step again (the dense comparator overwrote out / lse)
@@ -361,14 +364,11 @@ def run_gpu(args):
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     q_d, pt_d, sl_d = torch.empty_like(dw.q), torch.empty_like(dw.page_table), torch.empty_like(dw.seq_lens)
-    ws_sel = resident.workspace(binding.sv_quest_select_workspace_size(B, Hkv, max_pages), dev)
-
     def e2e_step():
         q_d.copy_(q_h, non_blocking=True)
         pt_d.copy_(pt_h, non_blocking=True)
         sl_d.copy_(sl_h, non_blocking=True)
-        binding.sv_quest_select(dw.cache, q_d, pt_d, sl_d, K, sel_idx, sel_cnt, workspace=ws_sel)
-        binding.sv_sparse_decode(dw.cache, q_d, pt_d, sl_d, sel_idx, sel_cnt, out, lse, ws)
+        binding.sv_quest_decode_step(dw.cache, q_d, pt_d, sl_d, K, sel_idx, sel_cnt, out, lse, ws_step)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
 
@@ -423,7 +423,8 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5)},
         "fused_step": {"ms_per_step": round(fused_ms, 5), "steps_per_s": round(1e3 / fused_ms, 2),
                        "agrees_with_step": fused_agree,
-                       "note": "sv_quest_decode_step: the same step as one cooperative launch, timed alone"},
+                       "note": "sv_quest_decode_step_single_launch: the same step as one cooperative launch, "
+                               "timed alone"},
         "fp8_step": {"ms_per_step": round(fp8_ms, 5), "steps_per_s": round(1e3 / fp8_ms, 2),
                      "bytes": ab["fp8_step"], "gbs": round(ab["fp8_step"] / (fp8_ms * 1e-3) / 1e9, 1),
                      "sparse_decode_ms": round(fp8_dec_ms, 5),

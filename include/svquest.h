@@ -8,7 +8,7 @@
  *   on_kv_stored(...)      -> sv_quest_update_meta  (store K/V, refresh page metadata)
  *   build_decode_view(q)   -> sv_quest_select       (query-aware page selection)
  *   generic attention      -> sv_sparse_decode      (attention over the view)
- * and sv_quest_decode_step runs the last two as one launch.
+ * and sv_quest_decode_step runs the last two in one call.
  *
  * Conventions common to every call
  *  - Every buffer argument is a DEVICE pointer, allocated and owned by the
@@ -80,8 +80,7 @@ enum sv_status {
  * back as value(code) * s.  The metadata stays bf16 and holds the min / max
  * of the keys as appended (before coding), so page selection is the same as
  * for bf16 pools; only attention reads the coded rows.  All calls accept both
- * formats except sv_quest_decode_step's single-launch kernel, which runs the
- * separate kernels for fp8 pools.
+ * formats except sv_quest_decode_step_single_launch (bf16 only).
  */
 typedef struct sv_cache {
     void* k_pool;             /* [num_phys_pages][num_kv_heads][16][128] of the format's element */
@@ -258,26 +257,18 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
                                     void* stream);
 
 /*
- * sv_quest_decode_step -- one decode step in a single kernel launch:
- * build_decode_view (page scores + top-K, as sv_quest_select) followed by
- * attention over the view (as sv_sparse_decode): the decode-time hooks of
- * the SparseEngine page ("method key points": query-relevant page selection
- * before attention, then attention over the selected pages only) fused into
- * one kernel.  The pages prescribe no kernel fusion; this is the same
- * computation scheduled as one launch.  Results are those of
- * sv_quest_select + sv_sparse_decode on the same inputs: sel_idx / sel_cnt
- * identical up to page scores that differ only in fp32 rounding order, out /
- * lse equal up to the split-K summation order.
+ * sv_quest_decode_step -- one decode step in one call: build_decode_view
+ * (page scores + top-K, exactly sv_quest_select) followed by attention over
+ * the view (exactly sv_sparse_decode), the decode-time hooks of the
+ * SparseEngine page ("method key points": query-relevant page selection
+ * before attention, then attention over the selected pages only).  It
+ * enqueues the same four kernels back to back with programmatic dependent
+ * launch.
  *  - budget_pages >= 1 is the row length of sel_idx, as in sv_quest_select.
  *  - softmax_scale > 0, as in sv_sparse_decode.
  *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
  *    with a call that may run at the same time; nothing in it needs to start
- *    at zero (the call clears its own counters first).
- *  - max_pages <= 8192 (131072 tokens) on a bf16 pool runs as one
- *    cooperative launch: every CTA co-resident, so the call returns
- *    SV_ERR_CUDA if the device cannot hold the grid (e.g. another context
- *    holds its SMs under MPS).  Larger max_pages, and fp8 pools, run
- *    sv_quest_select then sv_sparse_decode inside the same workspace.
+ *    at zero.
  */
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
                          const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
@@ -285,6 +276,28 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
                          int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * sv_quest_decode_step_single_launch -- the same step as ONE persistent
+ * cooperative kernel (scoring, top-K, split attention and combine scheduled
+ * inside the launch; the pages prescribe no fusion).  Results: sel_idx /
+ * sel_cnt identical to sv_quest_decode_step's up to page scores that differ
+ * only in fp32 rounding order, out / lse equal up to the split-K summation
+ * order.  Arguments and workspace as sv_quest_decode_step (the call clears its
+ * own counters first).  bf16 pools with max_pages <= 8192 (131072 tokens)
+ * only, else SV_ERR_UNSUPPORTED.  Every CTA must be co-resident: the call
+ * returns SV_ERR_CUDA if the device cannot hold the grid (e.g. another
+ * context holds its SMs under MPS).  It is slower than sv_quest_decode_step
+ * (on GB300, 8 requests of 128000 tokens: about 92 us against 52 us): its
+ * scoring CTAs share each SM's shared memory with attention stages, so fewer
+ * metadata bytes are in flight.  It serves callers that need one launch.
+ */
+int sv_quest_decode_step_single_launch(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                                       const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                       int32_t max_pages, int32_t budget_pages, float softmax_scale,
+                                       int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* Enough workspace for both step calls. */
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t max_pages, int32_t budget_pages);
 

@@ -248,10 +248,13 @@ size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, i
     return fused > separate ? fused : separate;
 }
 
-int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
-                         const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
-                         float softmax_scale, int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
-                         void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+int step_checks(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages, float softmax_scale,
+                const int32_t* sel_idx, const int32_t* sel_cnt, const void* out, const float* lse,
+                const void* workspace, size_t workspace_bytes) {
     int st = check_cache(cache);
     if (st) return st;
     if ((st = check_heads(cache, num_q_heads))) return st;
@@ -264,13 +267,23 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
         workspace_bytes < sv_quest_decode_step_workspace_size(batch, num_q_heads, cache->num_kv_heads, max_pages,
                                                               budget_pages))
         return SV_ERR_WORKSPACE;
+    return SV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads, const int32_t* page_table,
+                         const int32_t* seq_lens, int32_t batch, int32_t max_pages, int32_t budget_pages,
+                         float softmax_scale, int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    int st = step_checks(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, softmax_scale,
+                         sel_idx, sel_cnt, out, lse, workspace, workspace_bytes);
+    if (st) return st;
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (max_pages <= kMaxStepPages && cache->kv_format == SV_KV_BF16)
-        return launch_step(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, sel_idx,
-                           sel_cnt, softmax_scale, out, lse, workspace, workspace_bytes, sms, s);
-    // Separate kernels: scores at the front of the workspace, split-K partials after.
+    // Scores at the front of the workspace, split-K partials after.
     const size_t sb = scores_bytes(batch, cache->num_kv_heads, max_pages);
     float* scores = static_cast<float*>(workspace);
     if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s)))
@@ -280,6 +293,21 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
     return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
                          budget_pages, false, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
                          workspace_bytes - sb, sms, s);
+}
+
+int sv_quest_decode_step_single_launch(const sv_cache* cache, const void* q, int32_t num_q_heads,
+                                       const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
+                                       int32_t max_pages, int32_t budget_pages, float softmax_scale,
+                                       int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    int st = step_checks(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, softmax_scale,
+                         sel_idx, sel_cnt, out, lse, workspace, workspace_bytes);
+    if (st) return st;
+    if (max_pages > kMaxStepPages || cache->kv_format != SV_KV_BF16) return SV_ERR_UNSUPPORTED;
+    int sms = 0;
+    if ((st = sm_count_of_current_device(&sms))) return st;
+    return launch_step(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages, sel_idx, sel_cnt,
+                       softmax_scale, out, lse, workspace, workspace_bytes, sms, static_cast<cudaStream_t>(stream));
 }
 
 int sv_get_device_error(uint32_t* flags, int reset) {

@@ -128,7 +128,7 @@ def test_fp8_head_geometries(hq, hkv):
 
 
 def test_fp8_decode_step_and_error_vs_bf16():
-    """sv_quest_decode_step on an fp8 pool (separate kernels) matches the oracle;
+    """sv_quest_decode_step on an fp8 pool matches the oracle;
     the fp8 outputs stay close to the bf16 pool's (a statistic of the codec)."""
     spec = synth.SPECS[1].scaled(batch=2, ctx=16 * 300 + 3, budget_pages=40)
     wl, dw, host = _pair(spec)
@@ -140,6 +140,10 @@ def test_fp8_decode_step_and_error_vs_bf16():
     ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, spec.num_kv_heads,
                                                                         dw.page_table.shape[1], K))
     binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse, ws)
+    with pytest.raises(binding.SvError) as e:   # the single launch is bf16-only
+        binding.sv_quest_decode_step_single_launch(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx,
+                                                   sel_cnt, out, lse, ws)
+    assert e.value.status == 2
     sel, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
     o8, l8 = out.float().cpu().numpy(), lse.cpu().numpy()
     check_attention(o8, l8, *oracle.decode(host, wl.q, wl.page_table, wl.seq_lens, sel, cnt))

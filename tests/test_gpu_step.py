@@ -1,5 +1,7 @@
-"""sv_quest_decode_step (page scores, top-K and sparse attention in one launch)
-against the CPU oracle on the same seeded inputs.
+"""The single-launch step (sv_quest_decode_step_single_launch: page scores,
+top-K and sparse attention in one cooperative kernel) and the one-call step
+(sv_quest_decode_step: the same kernels as select + decode) against the CPU
+oracle on the same seeded inputs.
 
 Same bars as the separate calls: selected page sets exact except near-ties
 (fp32 scores within 1e-4 relative of the K-th score); bf16 outputs within
@@ -31,7 +33,7 @@ def _built(cuda_ok):
     assert binding.sv_get_device_error(reset=True) == 0
 
 
-def gpu_step(dw, budget_pages, page_table=None, q=None):
+def gpu_step(dw, budget_pages, page_table=None, q=None, single_launch=True):
     q = dw.q if q is None else q
     pt = dw.page_table if page_table is None else page_table
     B, Hq, D = q.shape
@@ -43,7 +45,8 @@ def gpu_step(dw, budget_pages, page_table=None, q=None):
     nbytes = binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, pt.shape[1], budget_pages)
     # Garbage in the workspace: the call must not rely on it starting at zero.
     ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
-    binding.sv_quest_decode_step(dw.cache, q, pt, dw.seq_lens, budget_pages, sel_idx, sel_cnt, out, lse, ws)
+    call = binding.sv_quest_decode_step_single_launch if single_launch else binding.sv_quest_decode_step
+    call(dw.cache, q, pt, dw.seq_lens, budget_pages, sel_idx, sel_cnt, out, lse, ws)
     return (sel_idx.cpu().numpy(), sel_cnt.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy())
 
 
@@ -128,9 +131,9 @@ def test_step_full_row_of_8192_pages():
     check_step(host, wl, gpu_step(dw, 100), 100)
 
 
-def test_step_wide_page_table_takes_two_stage_path():
-    """max_pages above 8192 runs select then decode inside the step's workspace;
-    results are the same as the fused launch on the narrow table."""
+def test_step_wide_page_table():
+    """max_pages above 8192: the one-call step handles it, the single launch
+    refuses it (SV_ERR_UNSUPPORTED) before launching anything."""
     spec = synth.SPECS[1].scaled(batch=3, ctx=16 * 700 + 9, budget_pages=40)
     wl = synth.make_workload(spec)
     dw = resident.upload(wl)
@@ -139,10 +142,19 @@ def test_step_wide_page_table_takes_two_stage_path():
     wide = np.full((B, 8300), -1, np.int32)
     wide[:, :width] = wl.page_table
     wide_t = torch.from_numpy(wide).cuda()
-    r_wide = gpu_step(dw, 40, page_table=wide_t)
+    r_wide = gpu_step(dw, 40, page_table=wide_t, single_launch=False)
     check_step(host, wl, r_wide, 40, page_table=wide)
-    r_narrow = gpu_step(dw, 40)
-    assert np.array_equal(r_wide[1], r_narrow[1])
+    with pytest.raises(binding.SvError) as e:
+        gpu_step(dw, 40, page_table=wide_t)
+    assert e.value.status == 2
+
+
+@pytest.mark.parametrize("cfg", [0, 2])
+def test_one_call_step_parity(cfg):
+    """sv_quest_decode_step (score, top-K, split decode, combine) vs the oracle."""
+    pr = pair(cfg)
+    K = pr.wl.spec.budget_pages
+    check_step(pr.host, pr.wl, gpu_step(pr.dw, K, single_launch=False), K)
 
 
 def test_step_exact_ties_go_to_lower_pages():

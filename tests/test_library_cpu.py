@@ -167,6 +167,17 @@ def test_decode_step_rejects_bad_args(lib):
     assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
 
 
+def test_single_launch_step_limits(lib):
+    def call(cache, max_pages=100):
+        ws = binding.sv_quest_decode_step_workspace_size(8, 32, 4, max_pages, 16)
+        return lib.sv_quest_decode_step_single_launch(cache, FAKE, 32, FAKE, FAKE, 8, max_pages, 16, 0.088, FAKE,
+                                                      FAKE, FAKE, FAKE, FAKE, ws, None)
+    assert call(ctypes.byref(_fake_cache()), max_pages=9000) == SV_ERR_UNSUPPORTED   # rows above 8192 pages
+    c8 = _fake_cache()
+    c8.kv_format, c8.k_scale, c8.v_scale = binding.SV_KV_FP8_E4M3, 0x10000, 0x10000
+    assert call(ctypes.byref(c8)) == SV_ERR_UNSUPPORTED                              # bf16 pools only
+
+
 def test_select_ex_and_decode_ex_option_checks(lib):
     c = ctypes.byref(_fake_cache())
 
