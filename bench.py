@@ -6,17 +6,16 @@ request), budget 4096 tokens (256 pages), 64 planted needle pages per request,
 physical pages shuffled over one pool; bf16 K/V/q, seeded synthetic data.
 
 A step is one attention layer's decode for the whole batch: page scoring,
-top-K selection and split-K attention over the selected pages
-(sv_quest_score + sv_quest_topk + sv_sparse_decode, the same kernels as
-sv_quest_select + sv_sparse_decode), captured once as a CUDA graph and
-replayed.  Inputs are resident in HBM; L2 is flushed before every timed step;
-each step is bracketed by CUDA events on the launching stream, all K steps
-are enqueued before one synchronisation, and the K step times are summed.
-Per-kernel durations come from a second pass that times each call alone.
-The end-to-end figure goes through the public one-call step
-(sv_quest_decode_step: the same four kernels) with q, page table and lengths
-copied in from pinned host memory and out / lse copied back inside the timed
-region.
+top-K selection and split-K attention over the selected pages, through the
+public one-call step sv_quest_decode_step (four kernels: scores, top-K, split
+decode, log-sum-exp combine, chained by programmatic dependent launch),
+captured once as a CUDA graph and replayed.  Inputs are resident in HBM; L2 is flushed before every
+timed step; each step is bracketed by CUDA events on the launching stream, all
+K steps are enqueued before one synchronisation, and the K step times are
+summed.  Per-kernel durations come from a second pass that times the separate
+calls (sv_quest_score, sv_quest_topk, sv_sparse_decode) alone.  The
+end-to-end figure runs the same call with q, page table and lengths copied in
+from pinned host memory and out / lse copied back inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -174,7 +173,7 @@ def algorithmic_bytes(wl):
 # sv_quest_update_meta one.
 KERNELS_PER_CALL = {"sv_quest_score": 1, "sv_quest_topk": 1, "sv_sparse_decode": 2, "sv_quest_decode_step": 4,
                     "sv_quest_decode_step_single_launch": 1, "sv_quest_update_meta": 1}
-STEP_CALLS = ("sv_quest_score", "sv_quest_topk", "sv_sparse_decode")
+STEP_CALLS = ("sv_quest_decode_step",)
 
 
 # ---------------------------------------------------------------- GPU arm
@@ -233,10 +232,11 @@ def run_gpu(args):
         binding.sv_sparse_decode(dw.cache, dw.q if q is None else q, dw.page_table if pt is None else pt,
                                  dw.seq_lens if sl is None else sl, sel_idx, sel_cnt, out, lse, ws)
 
+    ws_step = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, max_pages, K), dev)
+
     def step():
-        score()
-        topk()
-        decode()
+        binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse,
+                                     ws_step)
 
     def dense():
         binding.sv_sparse_decode(dw.cache, dw.q, dw.page_table, dw.seq_lens, None, None, out, lse, ws_dense)
@@ -308,14 +308,14 @@ def run_gpu(args):
     # ---- the same step as one cooperative launch (sv_quest_decode_step_single_launch)
     sel2, cnt2 = resident.select_buffers(B, Hkv, K, dev)
     out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
-    ws_step = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, max_pages, K), dev)
+    ws_single = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, max_pages, K), dev)
 
     def fused():
         binding.sv_quest_decode_step_single_launch(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel2, cnt2, out2,
-                                                   lse2, ws_step)
+                                                   lse2, ws_single)
 
     fused()
-    step()   # the three-call step again (the dense comparator overwrote out / lse)
+    step()   # the step again (the dense comparator overwrote out / lse)
     torch.cuda.synchronize(dev)
     fused_agree = bool(torch.equal(cnt2, sel_cnt)) and float((out2.float() - out.float()).abs().max()) <= 2e-2
     fused_ms = float(np.mean(timed(fused, max(3, min(args.steps, 200)))))
@@ -338,9 +338,8 @@ def run_gpu(args):
     out8, lse8 = torch.empty_like(out), torch.empty_like(lse)
 
     def step8():
-        binding.sv_quest_score(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, scores)
-        binding.sv_quest_topk(scores, dw8.seq_lens, K, sel8, cnt8)
-        binding.sv_sparse_decode(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, sel8, cnt8, out8, lse8, ws)
+        binding.sv_quest_decode_step(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, K, sel8, cnt8, out8, lse8,
+                                     ws_step)
 
     for _ in range(3):
         step8()
@@ -435,8 +434,8 @@ def run_gpu(args):
                            "gbs": round(append_bytes / (append_ms * 1e-3) / 1e9, 1)},
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
-        "gpu_launches_source": "kernels per call (score 1 + top-K 1 + split decode 1 + combine 1), counted "
-                               "by construction: the timed region replays a graph of exactly these calls",
+        "gpu_launches_source": "kernels per call (sv_quest_decode_step: score 1 + top-K 1 + split decode 1 + combine 1), "
+                               "counted by construction: the timed region replays a graph of exactly this call",
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:

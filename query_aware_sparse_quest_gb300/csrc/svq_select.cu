@@ -49,6 +49,7 @@ struct ScoreShape {
     // waiting on the slot's barrier for a later phase would see that phase's
     // parity as already complete.
     static_assert(kSlots % kScoreConsumers == 0, "ring slots must be a multiple of the consumer warps");
+    static_assert(kSlots <= kScoreThreads, "one thread initialises each slot's barriers");
 };
 
 // Warp-specialised streaming of page metadata.  Each CTA owns a contiguous
@@ -88,23 +89,28 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const int warp = threadIdx.x >> 5;
     const uint32_t full0 = smem_addr(&full_bar[0]);
     const uint32_t empty0 = smem_addr(&empty_bar[0]);
+    const int cta_begin = blockIdx.x * pages_per_cta;
 
-    if (threadIdx.x == 0) {
-        for (int st = 0; st < kSlots; ++st) {
-            mbar_init(full0 + st * 8, 1);
-            mbar_init(empty0 + st * 8, 1);
-        }
+    // The page table, like q and the lengths, is an input of the step.  The
+    // producer's first 32 entries (inside the table's row whatever the
+    // request's length) load together with the length, so the first copies
+    // wait for one memory round trip, not two.
+    const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
+    int nxt = (warp == kScoreProducer && cta_begin + lane < max_pages) ? pt_row[lane] : 0;
+    const int len = seq_lens[b];
+
+    if (threadIdx.x < kSlots) {
+        mbar_init(full0 + threadIdx.x * 8, 1);
+        mbar_init(empty0 + threadIdx.x * 8, 1);
         mbar_init_fence();
     }
     __syncthreads();
 
-    const int len = seq_lens[b];
     int n = (len + kPage - 1) / kPage;
     if (len < 1 || n > max_pages) {
         if (threadIdx.x == 0 && blockIdx.x == 0) svq_flag(SV_DEVERR_SEQ_LEN);
         n = len < 1 ? 0 : max_pages;
     }
-    const int cta_begin = blockIdx.x * pages_per_cta;
     const int span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
 
     if (warp != kScoreProducer) {
@@ -133,10 +139,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
     }
-    // The page table, like q and the lengths, is an input of the step: the
-    // producer's first entries load before the wait below.
-    const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
-    int nxt = (warp == kScoreProducer && lane < span) ? pt_row[lane] : 0;
     // Metadata may come from an append launched just before, and the previous
     // step's top-K may still read the score buffer.
     pdl_wait();

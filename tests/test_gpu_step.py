@@ -1,7 +1,8 @@
 """The single-launch step (sv_quest_decode_step_single_launch: page scores,
 top-K and sparse attention in one cooperative kernel) and the one-call step
-(sv_quest_decode_step: the same kernels as select + decode) against the CPU
-oracle on the same seeded inputs.
+(sv_quest_decode_step: the same kernels as select + decode, in one call)
+against the CPU oracle on the same seeded inputs.  Every test runs both
+calls.
 
 Same bars as the separate calls: selected page sets exact except near-ties
 (fp32 scores within 1e-4 relative of the K-th score); bf16 outputs within
@@ -33,7 +34,10 @@ def _built(cuda_ok):
     assert binding.sv_get_device_error(reset=True) == 0
 
 
-def gpu_step(dw, budget_pages, page_table=None, q=None, single_launch=True):
+CALLS = pytest.mark.parametrize("single_launch", [True, False], ids=["single_launch", "one_call"])
+
+
+def gpu_step(dw, budget_pages, page_table=None, q=None, single_launch=True, ws=None):
     q = dw.q if q is None else q
     pt = dw.page_table if page_table is None else page_table
     B, Hq, D = q.shape
@@ -43,8 +47,9 @@ def gpu_step(dw, budget_pages, page_table=None, q=None, single_launch=True):
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
     nbytes = binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, pt.shape[1], budget_pages)
-    # Garbage in the workspace: the call must not rely on it starting at zero.
-    ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
+    if ws is None:
+        # Garbage in the workspace: the call must not rely on it starting at zero.
+        ws = torch.full((nbytes,), 0xA5, dtype=torch.uint8, device="cuda")
     call = binding.sv_quest_decode_step_single_launch if single_launch else binding.sv_quest_decode_step
     call(dw.cache, q, pt, dw.seq_lens, budget_pages, sel_idx, sel_cnt, out, lse, ws)
     return (sel_idx.cpu().numpy(), sel_cnt.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy())
@@ -60,22 +65,31 @@ def check_step(host, wl, result, K, q=None, seq_lens=None, page_table=None):
     check_attention(out, lse, *oracle.decode(host, q, pt, seq, sel, cnt))
 
 
+@CALLS
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
-def test_step_parity(cfg):
+def test_step_parity(cfg, single_launch):
     pr = pair(cfg)
     K = pr.wl.spec.budget_pages
-    check_step(pr.host, pr.wl, gpu_step(pr.dw, K), K)
+    check_step(pr.host, pr.wl, gpu_step(pr.dw, K, single_launch=single_launch), K)
 
 
-def test_step_repeatable_and_matches_separate_calls():
-    """Two launches give bitwise equal results (the counters restart every
-    call), and they agree with sv_quest_select + sv_sparse_decode."""
+@CALLS
+def test_step_repeatable_and_matches_separate_calls(single_launch):
+    """Three launches give bitwise equal results, the last two on the
+    workspace the first left behind (the counters restart every call), and
+    they agree with sv_quest_select + sv_sparse_decode."""
     pr = pair(2)
     K = pr.wl.spec.budget_pages
-    r1 = gpu_step(pr.dw, K)
-    r2 = gpu_step(pr.dw, K)
-    for a, b in zip(r1, r2):
-        assert np.array_equal(a, b, equal_nan=True)
+    dw = pr.dw
+    B, Hq, D = dw.q.shape
+    ws = torch.full((binding.sv_quest_decode_step_workspace_size(B, Hq, dw.cache.num_kv_heads,
+                                                                 dw.page_table.shape[1], K),),
+                    0x5A, dtype=torch.uint8, device="cuda")
+    r1 = gpu_step(pr.dw, K, single_launch=single_launch)
+    for _ in range(2):
+        r2 = gpu_step(pr.dw, K, single_launch=single_launch, ws=ws)
+        for a, b in zip(r1, r2):
+            assert np.array_equal(a, b, equal_nan=True)
     dw = pr.dw
     B, Hq, D = dw.q.shape
     Hkv = dw.cache.num_kv_heads
@@ -94,18 +108,20 @@ def test_step_repeatable_and_matches_separate_calls():
     check_attention(r1[2], r1[3], out.float().cpu().numpy(), lse.cpu().numpy())
 
 
+@CALLS
 @pytest.mark.parametrize("hq,hkv", [(4, 1), (8, 1), (8, 2), (6, 2), (32, 4), (8, 8), (16, 8)])
-def test_step_head_geometries(hq, hkv):
+def test_step_head_geometries(hq, hkv, single_launch):
     spec = synth.Spec("geom", batch=3, num_q_heads=hq, num_kv_heads=hkv, ctx=0, ragged=(1, 900),
                       budget_pages=7, seed=hq * 10 + hkv + 1, outlier_channels=True, shuffle_pool=True)
     wl = synth.make_workload(spec)
     dw = resident.upload(wl)
     host = oracle.build_cache(wl, synth.UNFILLED_BITS)
     for K in (7, 64):
-        check_step(host, wl, gpu_step(dw, K), K)
+        check_step(host, wl, gpu_step(dw, K, single_launch=single_launch), K)
 
 
-def test_step_short_and_ragged_requests():
+@CALLS
+def test_step_short_and_ragged_requests(single_launch):
     """Single-token requests, exactly full pages, one-token last pages, n <= K
     (every page selected) and n > K, at budgets from 1 page up."""
     lens = np.array([1, 15, 16, 17, 31, 33, 16 * 40 + 1, 16 * 90], np.int32)
@@ -115,10 +131,11 @@ def test_step_short_and_ragged_requests():
     dw = resident.upload(wl)
     host = oracle.build_cache(wl, synth.UNFILLED_BITS)
     for K in (1, 2, 3, 17, 64, 200):
-        check_step(host, wl, gpu_step(dw, K), K)
+        check_step(host, wl, gpu_step(dw, K, single_launch=single_launch), K)
 
 
-def test_step_full_row_of_8192_pages():
+@CALLS
+def test_step_full_row_of_8192_pages(single_launch):
     """A request of exactly 8192 pages (the fused path's largest row) and a
     one-page request in the same batch."""
     lens = np.array([8192 * 16, 16 * 3 + 5], np.int32)
@@ -128,7 +145,7 @@ def test_step_full_row_of_8192_pages():
     dw = resident.upload(wl)
     assert dw.page_table.shape[1] == 8192
     host = oracle.build_cache(wl, synth.UNFILLED_BITS)
-    check_step(host, wl, gpu_step(dw, 100), 100)
+    check_step(host, wl, gpu_step(dw, 100, single_launch=single_launch), 100)
 
 
 def test_step_wide_page_table():
@@ -149,22 +166,15 @@ def test_step_wide_page_table():
     assert e.value.status == 2
 
 
-@pytest.mark.parametrize("cfg", [0, 2])
-def test_one_call_step_parity(cfg):
-    """sv_quest_decode_step (score, top-K, split decode, combine) vs the oracle."""
-    pr = pair(cfg)
-    K = pr.wl.spec.budget_pages
-    check_step(pr.host, pr.wl, gpu_step(pr.dw, K, single_launch=False), K)
-
-
-def test_step_exact_ties_go_to_lower_pages():
+@CALLS
+def test_step_exact_ties_go_to_lower_pages(single_launch):
     spec = synth.Spec("ties", batch=2, num_q_heads=32, num_kv_heads=4, ctx=16 * 300, budget_pages=37,
                       seed=6, shuffle_pool=True)
     wl = synth.make_workload(spec)
     k = wl.k_tok.reshape(2, 300, 16, 4, 128)
     k[:] = wl.k_tok[:16].copy()[None, None]
     dw = resident.upload(wl)
-    sel, cnt, out, lse = gpu_step(dw, 37)
+    sel, cnt, out, lse = gpu_step(dw, 37, single_launch=single_launch)
     for b in range(2):
         for g in range(4):
             assert sel[b, g].tolist() == list(range(37))
@@ -173,17 +183,19 @@ def test_step_exact_ties_go_to_lower_pages():
     check_attention(out, lse, *oracle.decode(host, wl.q, wl.page_table, wl.seq_lens, sel, cnt))
 
 
-def test_step_nan_in_unfilled_slots_is_masked():
+@CALLS
+def test_step_nan_in_unfilled_slots_is_masked(single_launch):
     spec = synth.SPECS[1].scaled(batch=3, ctx=16 * 50 + 3, budget_pages=9)
     wl = synth.make_workload(spec)
     dw = resident.upload(wl, fill_bits=0x7FC0)
     host = oracle.build_cache(wl, 0x7FC0)
-    res = gpu_step(dw, 9)
+    res = gpu_step(dw, 9, single_launch=single_launch)
     assert np.isfinite(res[2]).all() and np.isfinite(res[3]).all()
     check_step(host, wl, res, 9)
 
 
-def test_step_budget_sweep_after_append():
+@CALLS
+def test_step_budget_sweep_after_append(single_launch):
     """The full decode step of the budget-sweep workload: append one token per
     request, then the fused step at every budget of the sweep."""
     spec = synth.SPECS[4].scaled(batch=4, ctx=16 * 300 - 1)
@@ -198,4 +210,4 @@ def test_step_budget_sweep_after_append():
     dw.seq_lens.copy_(torch.from_numpy(seq))
     q = resident.bf16_tensor(wl.step_q[0], "cuda")
     for K in wl.spec.budget_sweep:
-        check_step(host, wl, gpu_step(dw, K, q=q), K, q=wl.step_q[0], seq_lens=seq)
+        check_step(host, wl, gpu_step(dw, K, q=q, single_launch=single_launch), K, q=wl.step_q[0], seq_lens=seq)
