@@ -133,7 +133,9 @@ int sv_quest_score(const sv_cache* cache, const void* q, int32_t num_q_heads,
  * For each (b, g) keeps the K_b = min(budget_pages, n_b) pages with the
  * highest score; among equal scores the lower logical page index wins.
  * Writes their logical indices in ascending order to sel_idx[b][g][0..K_b),
- * -1 to the rest of the row, and K_b to sel_cnt[b][g].
+ * -1 to the rest of the row, and K_b to sel_cnt[b][g].  Scores compare as
+ * fp32 values, except that -0.0 ranks below +0.0 and NaN above +inf
+ * (sv_quest_score produces neither from finite inputs).
  * max_pages <= 32768.
  */
 int sv_quest_topk(const float* scores, const int32_t* seq_lens, int32_t batch,

@@ -52,12 +52,13 @@ def _load():
         lib.oracle_quantize_rows.argtypes = [P, P, P, P, i64, i32, i32, i32, P, P, P, i64]
         lib.oracle_decode_fp8.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, P, P, i32, i32,
                                           f32, P, P]
+        lib.oracle_topk.argtypes = [P, P, i32, i32, i32, P, P]
         lib.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_value.restype = f32
         lib.oracle_e4m3_encode.argtypes = [f32]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
         for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode, lib.oracle_select_ex,
-                  lib.oracle_decode_ex, lib.oracle_quantize_rows, lib.oracle_decode_fp8):
+                  lib.oracle_decode_ex, lib.oracle_quantize_rows, lib.oracle_decode_fp8, lib.oracle_topk):
             f.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -146,6 +147,21 @@ def select(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.nda
     if rc != 0:
         raise ValueError(f"oracle_select failed ({rc})")
     return sel_idx, sel_cnt, scores
+
+
+def topk(scores: np.ndarray, n_pages: np.ndarray, budget_pages: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The selection step on given scores [rows][max_pages] with n_pages[row] valid entries:
+    returns (sel_idx [rows][K] ascending, -1 padded; sel_cnt [rows] = min(K, n))."""
+    scores = _c(scores, np.float32)
+    n_pages = _c(n_pages, np.int32)
+    rows, max_pages = scores.shape
+    K = int(budget_pages)
+    sel_idx = np.empty((rows, K), dtype=np.int32)
+    sel_cnt = np.empty((rows,), dtype=np.int32)
+    rc = _load().oracle_topk(_ptr(scores), _ptr(n_pages), rows, max_pages, K, _ptr(sel_idx), _ptr(sel_cnt))
+    if rc != 0:
+        raise ValueError(f"oracle_topk failed ({rc})")
+    return sel_idx, sel_cnt
 
 
 def decode(cache: Cache, q: np.ndarray, page_table: np.ndarray, seq_lens: np.ndarray,

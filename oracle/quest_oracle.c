@@ -211,6 +211,37 @@ int oracle_select_ex(const uint16_t* q, const uint16_t* meta,
     return 0;
 }
 
+/*
+ * The selection step alone, on given scores: for each of the rows, keep the
+ * min(K, n_pages[row]) pages of scores[row][0 .. n) that come first under
+ * (score desc, page asc) -- the order oracle_select_ex uses, with no forced
+ * pages -- and emit their indices ascending, padded with -1.
+ */
+int oracle_topk(const float* scores, const int32_t* n_pages, int rows, int max_pages, int K,
+                int32_t* sel_idx, int32_t* sel_cnt) {
+    if (K < 1 || rows < 0 || max_pages < 1) return -1;
+    scored_page* list = (scored_page*)malloc((size_t)max_pages * sizeof(scored_page));
+    if (!list) return -1;
+    for (int r = 0; r < rows; ++r) {
+        const int n = n_pages[r];
+        if (n < 0 || n > max_pages) { free(list); return -2; }
+        for (int p = 0; p < n; ++p) {
+            list[p].score = scores[(size_t)r * max_pages + p];
+            list[p].page = p;
+            list[p].forced = 0;
+        }
+        qsort(list, (size_t)n, sizeof(scored_page), by_score_then_index);
+        const int m = n < K ? n : K;
+        int32_t* out = sel_idx + (size_t)r * K;
+        for (int j = 0; j < m; ++j) out[j] = list[j].page;
+        qsort(out, (size_t)m, sizeof(int32_t), by_int_ascending);
+        for (int j = m; j < K; ++j) out[j] = -1;
+        sel_cnt[r] = m;
+    }
+    free(list);
+    return 0;
+}
+
 /* The base method: one row per kv group, no forced pages. */
 int oracle_select(const uint16_t* q, const uint16_t* meta,
                   const int32_t* page_table, const int32_t* seq_lens,

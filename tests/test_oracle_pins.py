@@ -200,6 +200,44 @@ def test_ranking_matches_bruteforce_subsets(seed):
     assert sel[0, 0, m:].tolist() == [-1] * (K - m)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_topk_alone_matches_bruteforce_subsets(seed):
+    """The selection step on given scores (oracle.topk): tiny rows drawn from a
+    few values (many exact ties, also +-inf): the selected set maximises the
+    score sum over all K-subsets and is the lexicographically smallest such
+    index set; indices ascend and the row is padded with -1."""
+    rng = np.random.default_rng(300 + seed)
+    rows, width = 5, 9
+    K = int(rng.integers(1, width + 2))
+    vals = np.array([-np.inf, -2.0, -0.5, 0.0, 0.5, 3.0, np.inf], np.float32)
+    scores = vals[rng.integers(0, len(vals), size=(rows, width))]
+    n = rng.integers(0, width + 1, size=rows).astype(np.int32)
+    sel, cnt = oracle.topk(scores, n, K)
+    for r in range(rows):
+        m = min(K, int(n[r]))
+        # the sum with infinities, compared exactly: more +inf first, then fewer -inf, then the finite sum
+        def key(c):
+            x = scores[r, list(c)]
+            return (int(np.sum(x == np.inf)), -int(np.sum(x == -np.inf)), float(np.sum(x[np.isfinite(x)])),
+                    [-i for i in c])
+        best = max(itertools.combinations(range(int(n[r])), m), key=key)
+        assert cnt[r] == m
+        assert sel[r, :m].tolist() == list(best)
+        assert sel[r, m:].tolist() == [-1] * (K - m)
+
+
+def test_topk_alone_agrees_with_select():
+    """oracle.topk on the scores oracle.select reports reproduces its selection."""
+    wl = synth.make_workload(synth.SPECS[1].scaled(batch=3, ctx=16 * 37 + 5, budget_pages=9))
+    host = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    sel, cnt, scores = oracle.select(host, wl.q, wl.page_table, wl.seq_lens, 9)
+    B, R, mp = scores.shape
+    n = np.repeat(-(-wl.seq_lens // 16), R).astype(np.int32)
+    sel2, cnt2 = oracle.topk(np.nan_to_num(scores.reshape(B * R, mp), nan=0.0), n, 9)
+    assert np.array_equal(sel2.reshape(B, R, 9), sel)
+    assert np.array_equal(cnt2.reshape(B, R), cnt)
+
+
 # ---------------------------------------------------------------- attention
 
 def _sdpa_fp64(q_heads, k, v, scale):
