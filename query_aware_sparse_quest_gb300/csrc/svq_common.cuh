@@ -177,9 +177,12 @@ inline int ceil_div(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) 
 
 // ---------------------------------------------------------------- programmatic dependent launch
 // Kernels of one step are launched so that the next kernel's CTAs may start
-// while the previous kernel drains.  Each kernel waits (griddepcontrol.wait)
-// before touching memory an earlier kernel of the library writes, and only
-// then lets its own dependents launch, so ordering stays transitive.
+// while the previous kernel drains.  Every CTA of every kernel waits
+// (griddepcontrol.wait) before it touches memory an earlier kernel of the
+// library writes and before it exits, so a kernel completes only after its
+// predecessor has, and ordering stays transitive.  Where a kernel lets its
+// dependents launch (griddepcontrol.launch_dependents) only decides when
+// their CTAs may be scheduled, never what they may read.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -73,12 +73,11 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // ring stage u and the split's pages u, u + 8, ...: after the consumers free
 // the stage, lane 4u publishes the page's valid-token count and arms the
 // stage's "full" mbarrier for 8 KB, and each of the group's four lanes moves
-// one box (K lo, K hi, V lo, V hi).  Each of the four consumer warps computes
-// the page's logits S^T = K Q^T for the whole query group (the same values in
-// every warp), runs the same online softmax and accumulates its own 32 output
-// channels O^T += V^T P^T, then arrives on the stage's "empty" mbarrier.
-// Because every consumer holds the same running max and sum, the CTA's
-// partial needs no cross-warp merge.
+// one box (K lo, K hi, V lo, V hi).  Consumer warp w takes the split's pages
+// w, w + 4, ... whole: the page's logits S^T = K Q^T for the query group, the
+// online softmax update and O^T += V^T P^T over all 128 channels, then it
+// arrives on the stage's "empty" mbarrier.  The four warps' running (max,
+// sum, output) are merged through shared memory into the CTA's partial.
 __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a,
                                                                           const __grid_constant__ CUtensorMap tmap_k,
                                                                           const __grid_constant__ CUtensorMap tmap_v) {

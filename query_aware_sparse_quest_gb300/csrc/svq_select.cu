@@ -105,6 +105,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         mbar_init_fence();
     }
     __syncthreads();
+    // The top-K kernel that follows may be scheduled now; its CTAs land as
+    // this kernel's CTAs retire, and wait for its completion to read scores.
+    pdl_launch_dependents();
 
     int n = (len + kPage - 1) / kPage;
     if (len < 1 || n > max_pages) {
@@ -173,7 +176,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         // This lane's copies land before the CTA (and its shared memory) retires.
         for (int p = issued_last; p >= 0 && p > issued_last - kSlots; p -= 32)
             (void)mbar_wait_bounded(full0 + (p % kSlots) * 8, (p / kSlots) & 1);
-        pdl_launch_dependents();
         return;
     }
 
@@ -352,8 +354,10 @@ __device__ __forceinline__ uint32_t order_key(float f) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Block-wide inclusive scan of one value per thread.  With reuse = false the
-// caller promises not to touch warp_tot again, which saves a barrier.
+// Block-wide inclusive scan of one value per thread: a warp scan, then each
+// warp adds up the totals of the warps before it, read after one barrier.
+// With reuse = false the caller promises that warp_tot is not written again
+// before the block's next barrier, which saves a second one.
 template <bool reuse = true>
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -364,17 +368,7 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
     }
     if (lane == 31) warp_tot[warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        uint32_t t = lane < kTopkWarps ? warp_tot[lane] : 0u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t x = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += x;
-        }
-        if (lane < kTopkWarps) warp_tot[lane] = t;
-    }
-    __syncthreads();
-    const uint32_t add = warp > 0 ? warp_tot[warp - 1] : 0u;
+    const uint32_t add = __reduce_add_sync(0xffffffffu, lane < warp ? warp_tot[lane] : 0u);
     if (reuse) __syncthreads();   // warp_tot may be reused right after
     return v + add;
 }
@@ -393,7 +387,8 @@ __device__ __forceinline__ void find_bin_from_top(const uint32_t* hist, uint32_t
         cnt[i] = hist[top - i];
         sum += cnt[i];
     }
-    uint32_t before = block_inclusive_scan(sum, warp_tot) - sum;   // keys in strictly higher bins
+    // warp_tot is next written after the barrier that ends this function.
+    uint32_t before = block_inclusive_scan<false>(sum, warp_tot) - sum;   // keys in strictly higher bins
 #pragma unroll
     for (int i = 0; i < kBinsPerThread; ++i) {
         if (before < remaining && remaining <= before + cnt[i]) {
@@ -436,11 +431,14 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     int32_t* out = sel_idx + static_cast<int64_t>(bg) * K;
     for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
     if (tid == 0) s_cand = 0u;
+    // The attention kernel that follows may start now: its CTAs set up and
+    // load q while this one runs, and wait for its completion before they
+    // read the selection.
+    pdl_launch_dependents();
     pdl_wait();   // scores come from the scoring kernel launched just before
     if (n <= K) {
         for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
         if (tid == 0) sel_cnt[bg] = n;
-        pdl_launch_dependents();
         return;
     }
 
@@ -502,26 +500,41 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         }
         __syncthreads();
         const int nc = static_cast<int>(s_cand);
-        if (tid < nc) {
-            // rank = keys above mine + equal keys at lower pages; the candidate
-            // ranked need - 1 is the threshold T, and the keys equal to T that
-            // are taken are those ranked at or before it: need - (keys above T).
-            const uint32_t my_k = cand_key[tid];
-            const int my_i = cand_idx[tid];
-            uint32_t above = 0, tied_before = 0;
+        // rank = keys above mine + equal keys at lower pages; the candidate
+        // ranked need - 1 is the threshold T, and the keys equal to T that are
+        // taken are those ranked at or before it: need - (keys above T).
+        auto rank = [&](int c, uint32_t& my_k, uint32_t& above) {
+            my_k = cand_key[c];
+            const int my_i = cand_idx[c];
+            uint32_t tied_before = 0;
+            above = 0;
             for (int j = 0; j < nc; ++j) {
                 const uint32_t kj = cand_key[j];
                 above += kj > my_k;
                 tied_before += (kj == my_k && cand_idx[j] < my_i);
             }
-            if (above + tied_before == need - 1) {
-                s_T = my_k;
-                s_take = need - above;
+            return above + tied_before == need - 1;
+        };
+        if (nc <= 32) {
+            // Few candidates (the usual case): every warp ranks them all, one
+            // per lane, so the threshold needs no further barrier.
+            uint32_t my_k = 0, above = 0;
+            const bool hit = lane < nc && rank(lane, my_k, above);
+            const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;   // exactly one candidate hits
+            T = __shfl_sync(0xffffffffu, my_k, src);
+            take = need - __shfl_sync(0xffffffffu, above, src);
+        } else {
+            if (tid < nc) {
+                uint32_t my_k, above;
+                if (rank(tid, my_k, above)) {
+                    s_T = my_k;
+                    s_take = need - above;
+                }
             }
+            __syncthreads();
+            T = s_T;
+            take = s_take;
         }
-        __syncthreads();
-        T = s_T;
-        take = s_take;
     } else {
         // 3b. many keys crowd one bin (e.g. equal scores): exact radix select.
         uint32_t prefix = 0, remaining = static_cast<uint32_t>(m);
@@ -577,7 +590,6 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     }
     for (int i = m + tid; i < K; i += kTopkThreads) out[i] = -1;
     if (tid == 0) sel_cnt[bg] = m;
-    pdl_launch_dependents();
 }
 
 int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
