@@ -66,18 +66,19 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// One CTA per (split, request, kv head).  The K and V pools are seen as 2-D
-// tensors [pages * kv heads * 16 rows][128 channels]; a page's 16 x 128 tile
-// of one kv head is two 16 x 64 TMA boxes (128-byte swizzle, so ldmatrix
-// reads are conflict-free).  Producer lane group u (lanes 4u .. 4u+3) owns
-// ring stage u and the split's pages u, u + 8, ...: after the consumers free
-// the stage, lane 4u publishes the page's valid-token count and arms the
-// stage's "full" mbarrier for 8 KB, and each of the group's four lanes moves
-// one box (K lo, K hi, V lo, V hi).  Consumer warp w takes the split's pages
-// w, w + 4, ... whole: the page's logits S^T = K Q^T for the query group, the
-// online softmax update and O^T += V^T P^T over all 128 channels, then it
-// arrives on the stage's "empty" mbarrier.  The four warps' running (max,
-// sum, output) are merged through shared memory into the CTA's partial.
+// One CTA per (split, request, kv head).  The K and V pools are seen as 3-D
+// tensors (64 channels, pages * kv heads * 16 rows, 2 channel halves); a
+// page's 16 x 128 tile of one kv head is one box that lands as two 16 x 64
+// halves, 128-byte swizzled (so ldmatrix reads are conflict-free).  Producer
+// lane group u (lanes 4u .. 4u+3) owns ring stage u and the split's pages
+// u, u + 8, ...: after the consumers free the stage, lane 4u publishes the
+// page's valid-token count, arms the stage's "full" mbarrier for 8 KB and
+// moves the K tile; lane 4u + 2 moves the V tile.  Consumer warp w takes the
+// split's pages w, w + 4, ... whole: the page's logits S^T = K Q^T for the
+// query group, the online softmax update and O^T += V^T P^T over all 128
+// channels, then it arrives on the stage's "empty" mbarrier.  The four warps'
+// running (max, sum, output) are merged through shared memory into the CTA's
+// partial.
 __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a,
                                                                           const __grid_constant__ CUtensorMap tmap_k,
                                                                           const __grid_constant__ CUtensorMap tmap_v) {
@@ -146,6 +147,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const uint32_t fb = full0 + u * 8;
         const uint32_t eb = empty0 + u * 8;
         const void* tmap = box < 2 ? static_cast<const void*>(&tmap_k) : static_cast<const void*>(&tmap_v);
+        const bool mover = (box & 1) == 0;         // lanes 4u (K) and 4u + 2 (V)
         const uint32_t dst = ring_s + u * kStageBytes + box * kBoxBytes;
         // Lane l resolves list position base + l to (physical page, valid
         // tokens); the next 32 are resolved while the current 32 are issued.
@@ -188,9 +190,9 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
                             if (phys >= 0) mbar_arrive_expect_tx(fb, kStageBytes);
                             else mbar_arrive(fb);
                         }
-                        if (phys >= 0) {
+                        if (phys >= 0 && mover) {
                             const int y = static_cast<int>((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * kPage);
-                            tma_load_2d(dst, tmap, (box & 1) * 64, y, fb);
+                            tma_load_3d(dst, tmap, 0, y, 0, fb);
                         }
                         last = i;
                     }
@@ -474,17 +476,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A pool bf16 [pages][kv heads][16][128] seen as a 2-D tensor
-// [pages * kv heads * 16 rows][128 channels], read in 16 x 64 boxes with the
-// 128-byte swizzle.
+// A pool bf16 [pages][kv heads][16][128] seen as a 3-D tensor: 64 channels
+// (contiguous), pages * kv heads * 16 rows (256 bytes apart), 2 channel
+// halves (128 bytes apart).  A box of 64 x 16 x 2 is one page's tile of one
+// kv head; in shared memory it lands as the low half's 16 rows, then the high
+// half's, each row of 128 bytes swizzled (128-byte swizzle).
 bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kPage)};
-    const cuuint32_t estride[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims, strides, box, estride,
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), 2};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kPage), 2};
+    const cuuint32_t estride[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides, box, estride,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
