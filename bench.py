@@ -15,7 +15,8 @@ K steps are enqueued before one synchronisation, and the K step times are
 summed.  Per-kernel durations come from a second pass that times the separate
 calls (sv_quest_score, sv_quest_topk, sv_sparse_decode) alone.  The
 end-to-end figure runs the same call with q, page table and lengths copied in
-from pinned host memory and out / lse copied back inside the timed region.
+from pinned host memory (one block, one copy) and out / lse copied back (one
+block, one copy) inside the timed region.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -357,23 +358,36 @@ def run_gpu(args):
                     + pages_touched * Hkv * 2 * D * 2)   # metadata written
 
     # ---- end to end through the public API: pinned host inputs in, results out
-    q_h = dw.q.cpu().pin_memory()
-    pt_h = dw.page_table.cpu().pin_memory()
-    sl_h = dw.seq_lens.cpu().pin_memory()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_d, pt_d, sl_d = torch.empty_like(dw.q), torch.empty_like(dw.page_table), torch.empty_like(dw.seq_lens)
+    # The step's inputs (q, page table, lengths) sit in one pinned host block
+    # and its results (out, lse) in one device block, so each direction is a
+    # single copy; the device tensors the call receives are views of them.
+    def packed(parts, device, pin):
+        offs, total = [], 0
+        for t in parts:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = torch.empty(total, dtype=torch.uint8, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for o, t in zip(offs, parts)]
+        return buf, views
+
+    in_h, (q_hv, pt_hv, sl_hv) = packed([dw.q, dw.page_table, dw.seq_lens], "cpu", True)
+    q_hv.copy_(dw.q.cpu())
+    pt_hv.copy_(dw.page_table.cpu())
+    sl_hv.copy_(dw.seq_lens.cpu())
+    in_d, (q_d, pt_d, sl_d) = packed([dw.q, dw.page_table, dw.seq_lens], dev, False)
+    res_d, (out_e, lse_e) = packed([out, lse], dev, False)
+    res_h = torch.empty(res_d.numel(), dtype=torch.uint8).pin_memory()
+
     def e2e_step():
-        q_d.copy_(q_h, non_blocking=True)
-        pt_d.copy_(pt_h, non_blocking=True)
-        sl_d.copy_(sl_h, non_blocking=True)
-        binding.sv_quest_decode_step(dw.cache, q_d, pt_d, sl_d, K, sel_idx, sel_cnt, out, lse, ws_step)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        in_d.copy_(in_h, non_blocking=True)
+        binding.sv_quest_decode_step(dw.cache, q_d, pt_d, sl_d, K, sel_idx, sel_cnt, out_e, lse_e, ws_step)
+        res_h.copy_(res_d, non_blocking=True)
 
     e2e_ms = max_over_ranks(float(np.mean(timed(e2e_step, max(3, min(args.steps, 200))))), dev)
-    h2d = q_h.numel() * 2 + pt_h.numel() * 4 + sl_h.numel() * 4
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    h2d = in_h.numel()
+    d2h = res_h.numel()
 
     torch.cuda.synchronize(dev)
     flags = binding.sv_get_device_error(reset=True)
