@@ -457,6 +457,112 @@ def run_gpu(args):
     return res
 
 
+# ---------------------------------------------------------------- every workload (--all-configs)
+
+def step_bytes(wl, budget_pages, appended=0):
+    """Algorithmic bytes of one step at a budget: metadata + selected K/V + page
+    table + q / out / lse (+ the appended tokens' K/V, pool rows and metadata)."""
+    s = wl.spec
+    P, Hkv, Hq, D = s.page_size, s.num_kv_heads, s.num_q_heads, s.head_dim
+    n = (wl.seq_lens.astype(np.int64) + appended + P - 1) // P
+    sel = np.minimum(n, budget_pages)
+    b = (int(n.sum()) * Hkv * 2 * D * 2 + int(sel.sum()) * Hkv * P * D * 2 * 2 + int(n.sum()) * 4
+         + s.batch * Hq * D * 2 + s.batch * Hq * (D * 2 + 4))
+    if appended:
+        b += appended * s.batch * Hkv * D * 2 * (2 + 2) + appended * s.batch * Hkv * 2 * D * 2
+    return b
+
+
+def run_all_configs(args):
+    """One JSON line per workload: the step (sv_quest_decode_step, CUDA graph,
+    L2 flushed before each replay, median of the timed replays) and the dense
+    all-pages decode, with algorithmic GB/s.  The append + sweep workload appends
+    one token per request (sv_quest_update_meta) before the step, at each budget
+    of the sweep."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    peak, _ = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn, n, warm):
+        for _ in range(warm):
+            flush_w.zero_(); flush_r.sum(); fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        torch.cuda.synchronize(dev)
+        for e0, e1 in evs:
+            flush_w.zero_(); flush_r.sum()
+            e0.record(); fn(); e1.record()
+        torch.cuda.synchronize(dev)
+        return float(np.median([e0.elapsed_time(e1) for e0, e1 in evs]))
+
+    def graph_of(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            fn(); fn()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize(dev)
+        return g
+
+    n_timed, n_warm = max(20, min(args.steps, 200)), max(3, min(args.warmup, 20))
+    for cfg, spec in synth.SPECS.items():
+        wl = synth.make_workload(spec)
+        dw = resident.upload(wl, device=dev)
+        B, Hq, D = dw.q.shape
+        Hkv = spec.num_kv_heads
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        line = {"config": spec.name, "batch": B, "max_pages": wl.max_pages, "pool": "shuffled" if spec.shuffle_pool
+                else "contiguous"}
+        appended = 0
+        q = dw.q
+        pre = None
+        if spec.append_steps:
+            appended = 1
+            k1 = resident.bf16_tensor(wl.step_k[0], dev)
+            v1 = resident.bf16_tensor(wl.step_v[0], dev)
+            s1 = torch.from_numpy(wl.step_slots[0]).to(dev)
+            dw.seq_lens.copy_(torch.from_numpy(wl.seq_lens_after(1)))
+            q = resident.bf16_tensor(wl.step_q[0], dev)
+
+            def pre():
+                binding.sv_quest_update_meta(dw.cache, k1, v1, s1)
+        budgets = spec.budget_sweep or (spec.budget_pages,)
+        steps = []
+        for K in budgets:
+            sel, cnt = resident.select_buffers(B, Hkv, K, dev)
+            ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, wl.max_pages, K), dev)
+
+            def step(K=K, sel=sel, cnt=cnt, ws=ws):
+                if pre is not None:
+                    pre()
+                binding.sv_quest_decode_step(dw.cache, q, dw.page_table, dw.seq_lens, K, sel, cnt, out, lse, ws)
+
+            ms = timed(graph_of(step).replay, n_timed, n_warm)
+            nb = step_bytes(wl, K, appended)
+            steps.append({"budget_pages": K, "us": round(ms * 1e3, 2), "steps_per_s": round(1e3 / ms, 1),
+                          "bytes": nb, "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                          "frac_of_measured": round(nb / (ms * 1e-3) / 1e9 / peak, 4)})
+            del sel, cnt, ws
+        wsd = resident.workspace(binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, wl.max_pages), dev)
+        dense = lambda: binding.sv_sparse_decode(dw.cache, q, dw.page_table, dw.seq_lens, None, None, out, lse, wsd)
+        ms = timed(graph_of(dense).replay, max(5, n_timed // 4), n_warm)
+        n_all = int(((wl.seq_lens.astype(np.int64) + appended + spec.page_size - 1) // spec.page_size).sum())
+        nd = n_all * Hkv * spec.page_size * D * 2 * 2 + n_all * 4 + B * Hq * (D * 2 + D * 2 + 4)
+        line["step"] = steps if len(steps) > 1 else steps[0]
+        line["dense"] = {"us": round(ms * 1e3, 2), "bytes": nd, "gbs": round(nd / (ms * 1e-3) / 1e9, 1)}
+        line["flags"] = binding.sv_get_device_error(reset=True)
+        print(json.dumps(line), flush=True)
+        del dw, out, lse, wsd
+        torch.cuda.empty_cache()
+
+
 # ---------------------------------------------------------------- CPU oracle (baseline / reference arm)
 
 def _oracle_host(wl):
@@ -526,8 +632,13 @@ def main():
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--all-configs", action="store_true",
+                    help="instead of the benchmark line, one line per workload (step and dense timings)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
+    if args.all_configs:
+        run_all_configs(args)
+        return
     res = run_reference(args) if args.impl == "reference" else run_gpu(args)
     if res is not None:
         print(json.dumps(res), flush=True)

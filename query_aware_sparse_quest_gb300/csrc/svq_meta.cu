@@ -24,6 +24,11 @@ __global__ void __launch_bounds__(256) append_kv_meta_kernel(
     const __nv_bfloat16* __restrict__ v_new, const int32_t* __restrict__ slot_mapping, int64_t num_tokens) {
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    // The kernel before may still read the pool and the metadata: wait for
+    // it before writing.  The scoring kernel that usually follows may then
+    // be scheduled and load its page-table entries and query meanwhile.
+    pdl_wait();
+    pdl_launch_dependents();
     if (item >= num_tokens * num_kv_heads) return;
     const int64_t t = item / num_kv_heads;
     const int h = static_cast<int>(item % num_kv_heads);
@@ -121,15 +126,16 @@ int launch_update_meta(const sv_cache* c, const void* k_new, const void* v_new, 
     const auto kn = static_cast<const __nv_bfloat16*>(k_new);
     const auto vn = static_cast<const __nv_bfloat16*>(v_new);
     auto* meta = static_cast<__nv_bfloat16*>(c->meta);
+    cudaError_t e;
     if (c->kv_format == SV_KV_FP8_E4M3)
-        append_kv_meta_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            c->k_pool, c->v_pool, meta, static_cast<float*>(c->k_scale), static_cast<float*>(c->v_scale),
-            c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping, num_tokens);
+        e = launch_pdl(append_kv_meta_kernel<true>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                       c->k_pool, c->v_pool, meta, static_cast<float*>(c->k_scale), static_cast<float*>(c->v_scale),
+                       c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping, num_tokens);
     else
-        append_kv_meta_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-            c->k_pool, c->v_pool, meta, nullptr, nullptr, c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping,
-            num_tokens);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+        e = launch_pdl(append_kv_meta_kernel<false>, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                       c->k_pool, c->v_pool, meta, static_cast<float*>(nullptr), static_cast<float*>(nullptr),
+                       c->num_phys_pages, c->num_kv_heads, kn, vn, slot_mapping, num_tokens);
+    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace svq

@@ -5,6 +5,8 @@
 //   score_pages_kernel : upper-bound score of every (request, kv head, page)
 //   topk_pages_kernel  : top-K pages per (request, kv head), ties to the lower
 //                        page index, emitted in ascending page order
+#include <algorithm>
+
 #include "svq_common.cuh"
 
 namespace svq {
@@ -35,6 +37,76 @@ SVQ_DEFINE_ERROR_WORD(read_error_select)
 constexpr int kScoreConsumers = SVQ_SCORE_CONSUMERS;
 constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
 constexpr int kScoreProducer = kScoreConsumers;   // warp index of the producer
+
+// The scoring grid over a batch of (possibly very different) request lengths:
+// with a one-dimensional grid of X >= B CTAs, request b gets
+// k_b = 1 + floor((X - B) n_b / N) CTAs (N = the batch's pages; sum k_b <= X)
+// that split its n_b pages evenly, so a CTA's load is at most about N / (X - B)
+// pages whatever the length mix; the CTAs past sum k_b have nothing to do.
+// Every warp works this out itself from the lengths (one coalesced load).
+// With equal lengths k_b = floor(X / B), the split of a two-dimensional grid.
+struct ScoreRun {
+    int b;       // request, -1: no pages for this CTA
+    int begin;   // first logical page
+    int span;    // pages
+    int n;       // the request's page count
+};
+
+constexpr int kLenSlots = 8;   // lengths a lane holds: the split by length serves up to 256 requests
+
+__device__ __forceinline__ int pages_of(int len, int max_pages, bool flag) {
+    int n = (len + kPage - 1) / kPage;
+    if (len < 1 || n > max_pages) {
+        if (flag) svq_flag(SV_DEVERR_SEQ_LEN);
+        n = len < 1 ? 0 : max_pages;
+    }
+    return n;
+}
+
+// lens[i] = the length of request lane + 32 i (loaded by the caller).
+__device__ __forceinline__ ScoreRun run_by_length(const int (&lens)[kLenSlots], int batch, int max_pages, int cta,
+                                                  int ctas, int lane, bool flag) {
+    int n_of[kLenSlots];
+    int64_t total = 0;
+#pragma unroll
+    for (int i = 0; i < kLenSlots; ++i) {
+        n_of[i] = lane + 32 * i < batch ? pages_of(lens[i], max_pages, flag) : 0;
+        total += n_of[i];
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) total += __shfl_xor_sync(0xffffffffu, total, o);
+    ScoreRun run = {-1, 0, 0, 0};
+    int before = 0;   // CTAs of the requests before this chunk
+#pragma unroll
+    for (int i = 0; i < kLenSlots; ++i) {
+        if (32 * i >= batch || run.b >= 0) break;   // warp-uniform
+        const int r = 32 * i + lane;
+        const int n = n_of[i];
+        const int k = r < batch ? 1 + (total > 0 ? static_cast<int>(static_cast<int64_t>(ctas - batch) * n / total) : 0)
+                                : 0;
+        int incl = k;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const bool mine = r < batch && cta >= before + incl - k && cta < before + incl;
+        const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            const int x = cta - (before + __shfl_sync(0xffffffffu, incl - k, src));
+            const int kb = __shfl_sync(0xffffffffu, k, src);
+            const int nb = __shfl_sync(0xffffffffu, n, src);
+            const int per = (nb + kb - 1) / kb;
+            run.b = 32 * i + src;
+            run.n = nb;
+            run.begin = x * per;
+            run.span = max(0, min(nb, run.begin + per) - run.begin);
+        }
+        before += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    return run;
+}
 
 template <int HKV>
 struct ScoreShape {
@@ -74,7 +146,7 @@ template <int HKV, bool PER_HEAD>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const __nv_bfloat16* __restrict__ meta, int64_t num_phys_pages, const __nv_bfloat16* __restrict__ q,
     int group, const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens, int max_pages,
-    int pages_per_cta, int sink, int window, float* __restrict__ scores) {
+    int pages_per_cta, int sink, int window, float* __restrict__ scores, int batch) {
     using S = ScoreShape<HKV>;
     constexpr int kSlots = S::kSlots, L = S::L, C = S::C;
     extern __shared__ __align__(128) unsigned char ring[];
@@ -84,12 +156,41 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     __shared__ unsigned char slot_ok[kSlots];
     __shared__ __align__(16) __nv_bfloat16 qstage[HKV * kMaxGroup * kHeadDim];
 
-    const int b = blockIdx.y;
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const uint32_t full0 = smem_addr(&full_bar[0]);
     const uint32_t empty0 = smem_addr(&empty_bar[0]);
-    const int cta_begin = blockIdx.x * pages_per_cta;
+
+    // A two-dimensional grid gives request blockIdx.y the runs of
+    // pages_per_cta pages; a one-dimensional grid splits the batch by length
+    // (run_by_length), and pages_per_cta is then the run its CTA has when all
+    // requests are full (floor(X / B) runs each), the guess under which the
+    // first page-table entries and the query are fetched before the lengths
+    // are known.
+    const bool by_length = gridDim.y == 1 && batch > 1;
+    int b = blockIdx.y;
+    int cta_begin = blockIdx.x * pages_per_cta;
+    if (by_length) {
+        const int per_req = gridDim.x / batch;
+        b = blockIdx.x / per_req;
+        cta_begin = (blockIdx.x % per_req) * pages_per_cta;
+        if (b >= batch) b = batch - 1, cta_begin = max_pages;   // no guess: fetched after the lengths
+    }
+    const int guess_b = b, guess_begin = cta_begin;
+    // Consumers fetch the (guessed) request's query, Hq x 128 bf16 (at most
+    // 16 KB), with 16-byte loads now, and keep it if the guess holds.
+    constexpr int kConsumerThreads = kScoreConsumers * 32;
+    constexpr int kQVecs = (HKV * kMaxGroup * kHeadDim / 8 + kConsumerThreads - 1) / kConsumerThreads;
+    const int hq = HKV * group;
+    uint4 qpre[kQVecs];
+    if (warp != kScoreProducer) {
+        const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
+#pragma unroll
+        for (int i = 0; i < kQVecs; ++i) {
+            const int v = threadIdx.x + i * kConsumerThreads;
+            qpre[i] = v < hq * kHeadDim / 8 ? qsrc[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
 
     // The page table, like q and the lengths, is an input of the step.  The
     // producer's first 32 entries (inside the table's row whatever the
@@ -98,6 +199,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const int32_t* pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
     int nxt = (warp == kScoreProducer && cta_begin + lane < max_pages) ? pt_row[lane] : 0;
     const int len = seq_lens[b];
+    int lens[kLenSlots];
+#pragma unroll
+    for (int i = 0; i < kLenSlots; ++i) lens[i] = by_length && lane + 32 * i < batch ? seq_lens[lane + 32 * i] : 0;
 
     if (threadIdx.x < kSlots) {
         mbar_init(full0 + threadIdx.x * 8, 1);
@@ -109,24 +213,52 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     // this kernel's CTAs retire, and wait for its completion to read scores.
     pdl_launch_dependents();
 
-    int n = (len + kPage - 1) / kPage;
-    if (len < 1 || n > max_pages) {
-        if (threadIdx.x == 0 && blockIdx.x == 0) svq_flag(SV_DEVERR_SEQ_LEN);
-        n = len < 1 ? 0 : max_pages;
+    int n, span;
+    bool all_full = by_length;   // every request fills the table's row: the guess is the split
+    if (by_length) {
+#pragma unroll
+        for (int i = 0; i < kLenSlots; ++i)
+            if (lane + 32 * i < batch) all_full &= lens[i] >= 1 && (lens[i] + kPage - 1) / kPage == max_pages;
+        all_full = __all_sync(0xffffffffu, all_full);
     }
-    const int span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
+    if (all_full) {
+        n = max_pages;
+        span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
+    } else if (by_length) {
+        const ScoreRun run = run_by_length(lens, batch, max_pages, blockIdx.x, gridDim.x, lane,
+                                           warp == 0 && blockIdx.x == 0);
+        n = run.n;
+        span = run.span;
+        b = run.b < 0 ? guess_b : run.b;
+        cta_begin = run.begin;
+        if (warp == kScoreProducer && (b != guess_b || cta_begin != guess_begin)) {
+            // Another split than the guess (unequal lengths): fetch the entries now.
+            pt_row = page_table + static_cast<int64_t>(b) * max_pages + cta_begin;
+            nxt = lane < span ? pt_row[lane] : 0;
+        }
+    } else {
+        n = (len + kPage - 1) / kPage;
+        if (len < 1 || n > max_pages) {
+            if (threadIdx.x == 0 && blockIdx.x == 0) svq_flag(SV_DEVERR_SEQ_LEN);
+            n = len < 1 ? 0 : max_pages;
+        }
+        span = max(0, min(n, cta_begin + pages_per_cta) - cta_begin);
+    }
 
     if (warp != kScoreProducer) {
-        // Consumers stage this request's query (Hq x 128 bf16, at most 16 KB)
-        // in shared memory with 16-byte loads and fold each kv group's query
-        // heads into Qp / Qn, while the producer already streams metadata.
-        // q is an input of the step, so this also overlaps the previous kernel.
-        constexpr int kConsumerThreads = kScoreConsumers * 32;
-        const int hq = HKV * group;
+        // Consumers stage this request's query in shared memory and fold each
+        // kv group's query heads into Qp / Qn, while the producer already
+        // streams metadata.  q is an input of the step, so this also overlaps
+        // the previous kernel.
         {
             const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
             uint4* qdst = reinterpret_cast<uint4*>(qstage);
-            for (int i = threadIdx.x; i < hq * kHeadDim / 8; i += kConsumerThreads) qdst[i] = qsrc[i];
+            const bool kept = b == guess_b;
+#pragma unroll
+            for (int i = 0; i < kQVecs; ++i) {
+                const int v = threadIdx.x + i * kConsumerThreads;
+                if (v < hq * kHeadDim / 8) qdst[v] = kept ? qpre[i] : qsrc[v];
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
         for (int idx = threadIdx.x; idx < HKV * kHeadDim; idx += kConsumerThreads) {
@@ -293,14 +425,29 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
             return SV_ERR_CUDA;
         if (dev < 64) attr_set[dev] = true;
     }
-    // One CTA per SM over the (batch x max_pages) page grid.
-    int64_t ppc = (static_cast<int64_t>(batch) * max_pages + sm_count - 1) / sm_count;
-    if (ppc < 32) ppc = 32;
-    const int ctas = ceil_div(max_pages, ppc);
-    const cudaError_t e = launch_pdl(score_pages_kernel<HKV, PER_HEAD>, dim3(ctas, batch), dim3(kScoreThreads),
-                                     S::kSmemBytes, stream, static_cast<const __nv_bfloat16*>(c->meta),
-                                     c->num_phys_pages, q, group, page_table, seq_lens, max_pages,
-                                     static_cast<int>(ppc), sink, window, scores);
+    // At most one wave of one CTA per SM.  Up to SM-count requests: a
+    // one-dimensional grid of X CTAs (at least 32 pages each when the
+    // requests are full) that the kernel splits by the actual lengths, and
+    // the run a CTA has when all requests are full (the kernel's guess).
+    // More requests: one CTA each, in waves.
+    dim3 grid;
+    int64_t ppc;
+    if (batch > 1 && batch <= sm_count && batch <= 32 * kLenSlots) {
+        const int64_t want = (static_cast<int64_t>(batch) * max_pages + 31) / 32;
+        const int X = static_cast<int>(std::min<int64_t>(sm_count, std::max<int64_t>(batch, want)));
+        const int per_req = X / batch;
+        ppc = (static_cast<int64_t>(max_pages) + per_req - 1) / per_req;
+        grid = dim3(X, 1);
+    } else {
+        const int per_req = max(1, sm_count / batch);
+        ppc = (static_cast<int64_t>(max_pages) + per_req - 1) / per_req;
+        if (ppc < 32) ppc = 32;
+        grid = dim3(ceil_div(max_pages, ppc), batch);
+    }
+    const cudaError_t e = launch_pdl(score_pages_kernel<HKV, PER_HEAD>, grid, dim3(kScoreThreads), S::kSmemBytes,
+                                     stream, static_cast<const __nv_bfloat16*>(c->meta), c->num_phys_pages, q, group,
+                                     page_table, seq_lens, max_pages, static_cast<int>(ppc), sink, window, scores,
+                                     batch);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
