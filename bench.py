@@ -546,9 +546,18 @@ def run_all_configs(args):
 
             ms = timed(graph_of(step).replay, n_timed, n_warm)
             nb = step_bytes(wl, K, appended)
-            steps.append({"budget_pages": K, "us": round(ms * 1e3, 2), "steps_per_s": round(1e3 / ms, 1),
-                          "bytes": nb, "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
-                          "frac_of_measured": round(nb / (ms * 1e-3) / 1e9 / peak, 4)})
+            entry = {"budget_pages": K, "us": round(ms * 1e3, 2), "steps_per_s": round(1e3 / ms, 1),
+                     "bytes": nb, "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_measured": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
+            if wl.max_pages <= 8192:
+                def single(K=K, sel=sel, cnt=cnt, ws=ws):
+                    if pre is not None:
+                        pre()
+                    binding.sv_quest_decode_step_single_launch(dw.cache, q, dw.page_table, dw.seq_lens, K, sel, cnt,
+                                                               out, lse, ws)
+
+                entry["single_launch_us"] = round(timed(graph_of(single).replay, n_timed, n_warm) * 1e3, 2)
+            steps.append(entry)
             del sel, cnt, ws
         wsd = resident.workspace(binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, wl.max_pages), dev)
         dense = lambda: binding.sv_sparse_decode(dw.cache, q, dw.page_table, dw.seq_lens, None, None, out, lse, wsd)
