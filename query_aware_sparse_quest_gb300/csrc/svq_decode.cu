@@ -20,7 +20,7 @@ namespace svq {
 
 SVQ_DEFINE_ERROR_WORD(read_error_decode)
 
-constexpr int kConsumers = 4;                     // consumer warps; warp w owns channels 32w .. 32w+31
+constexpr int kConsumers = 4;                     // consumer warps; warp w takes pages w, w + 4, ... of its split
 constexpr int kDecodeThreads = (kConsumers + 1) * 32;
 constexpr int kProducer = kConsumers;             // warp index of the producer
 constexpr int kStages = 8;                        // pages in flight per CTA (one producer lane group each)

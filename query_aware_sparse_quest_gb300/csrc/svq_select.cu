@@ -21,12 +21,10 @@ SVQ_DEFINE_ERROR_WORD(read_error_select)
 // turns the score into one fp32 multiply-add per metadata element (1 flop per
 // byte), which keeps the kernel bound by HBM rather than by the ALUs.
 //
-// A page's metadata for all kv heads is contiguous (HKV x 512 bytes).  Lane l
-// reads 16 bytes of every head j: chunk l of [kmin(128) | kmax(128)], so its
-// coefficients are fixed for the kernel's lifetime (Qn for l < 16, Qp for
-// l >= 16, channels 8 (l & 15) .. + 7).  Each warp keeps U pages x HKV heads of
-// 16-byte loads in flight and folds the U*HKV lane partials with a transposed
-// butterfly (one shuffle per score).
+// A page's metadata for all kv heads is contiguous (HKV x 512 bytes) and
+// reaches shared memory as one bulk copy; a consumer lane's coefficients
+// (its request's Qp or Qn over its channels) stay in registers for the
+// CTA's whole run of pages.
 
 #ifndef SVQ_SCORE_CONSUMERS
 #define SVQ_SCORE_CONSUMERS 8
@@ -475,7 +473,8 @@ int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_
 // ---------------------------------------------------------------- top-K
 //
 // One CTA per (request, kv head).  Scores become order-preserving 32-bit
-// keys in shared memory.  The threshold search is a selection, not a sort:
+// keys held in registers (each thread a run of consecutive pages).  The
+// threshold search is a selection, not a sort:
 //  1. one histogram over [min key, max key] in 2048 power-of-two-wide bins
 //     (a bin index is a right shift of key - min, so bins are monotone in the
 //     score) locates the bin b* holding the K-th best key;
