@@ -35,17 +35,20 @@ constexpr int kMaxStepPages = 8192;   // one top-K row per 256 threads x 32 keys
 namespace {
 
 int sm_count_of_current_device(int* out) {
-    static int cached[64] = {};
+    static std::atomic<int> cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-    if (dev >= 0 && dev < 64 && cached[dev] > 0) {
-        *out = cached[dev];
-        return SV_OK;
+    if (dev >= 0 && dev < 64) {
+        const int c = cached[dev].load(std::memory_order_acquire);
+        if (c > 0) {
+            *out = c;
+            return SV_OK;
+        }
     }
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
         return SV_ERR_CUDA;
-    if (dev >= 0 && dev < 64) cached[dev] = n;
+    if (dev >= 0 && dev < 64) cached[dev].store(n, std::memory_order_release);
     *out = n;
     return SV_OK;
 }

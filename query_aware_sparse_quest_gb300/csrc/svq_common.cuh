@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "svquest.h"
@@ -208,10 +209,38 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Per-device cache of one int (SM count, opt-in flags); index < 64.
 inline int current_device() {
     int dev = 0;
     return cudaGetDevice(&dev) == cudaSuccess ? dev : -1;
+}
+
+// One-time host set-up per device (a kernel attribute, a device query).  A
+// slot per device index below 64 remembers that it succeeded; larger indices
+// run it on every call.  The slots are atomics, so first calls from several
+// host threads at once each run the idempotent set-up without a data race.
+template <typename F>
+inline int once_per_device(std::atomic<bool> (&done)[64], F&& setup) {
+    const int dev = current_device();
+    if (dev < 0) return SV_ERR_CUDA;
+    if (dev < 64 && done[dev].load(std::memory_order_acquire)) return SV_OK;
+    const int st = setup();
+    if (st == SV_OK && dev < 64) done[dev].store(true, std::memory_order_release);
+    return st;
+}
+
+// The driver's cuTensorMapEncodeTiled (ABI version 12000), looked up once per
+// process (a function-local static, initialised thread-safely); null if the
+// driver does not provide it.
+inline void* tensor_map_encode_entry() {
+    static void* const fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        const bool ok = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                                         &qr) == cudaSuccess &&
+                        qr == cudaDriverEntryPointSuccess;
+        return ok ? p : nullptr;
+    }();
+    return fn;
 }
 
 }  // namespace svq

@@ -464,16 +464,7 @@ size_t decode_workspace_bytes(int batch, int num_q_heads, int splits) {
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_entry());
 }
 
 // A pool bf16 [pages][kv heads][16][128] seen as a 3-D tensor: 64 channels
@@ -505,15 +496,14 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                   const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
                   float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream) {
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
-    if (dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(flash_decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kDecodeSmem) != cudaSuccess)
-            return SV_ERR_CUDA;
-        attr_set[dev] = true;
-    }
+    static std::atomic<bool> attr_set[64];
+    const int st0 = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(flash_decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    kDecodeSmem) == cudaSuccess
+                   ? SV_OK
+                   : SV_ERR_CUDA;
+    });
+    if (st0) return st0;
     const int pages = sel_idx ? budget_pages : max_pages;
     if (c->kv_format == SV_KV_FP8_E4M3) {
         const bool per_head8 = per_q_head && sel_idx;

@@ -386,16 +386,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 f8_tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_entry());
 }
 
 // An e4m3 pool [pages][kv heads][16][128] as a 2-D byte tensor
@@ -416,15 +407,14 @@ bool encode_f8_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
 }  // namespace
 
 int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages, int sm_count, int max_splits) {
-    static bool attr_set[64] = {};
-    const int dev = current_device();
-    if (dev < 0) return -1;
-    if (dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(flash_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kF8Smem) !=
-            cudaSuccess)
-            return -1;
-        if (dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> attr_set[64];
+    if (once_per_device(attr_set, [] {
+            return cudaFuncSetAttribute(flash_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kF8Smem) == cudaSuccess
+                       ? SV_OK
+                       : SV_ERR_CUDA;
+        }) != SV_OK)
+        return -1;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, flash_decode_fp8_kernel, kF8Threads, kF8Smem) !=
             cudaSuccess ||

@@ -414,15 +414,14 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
                      const int32_t* seq_lens, int batch, int max_pages, int sink, int window, float* scores,
                      int sm_count, cudaStream_t stream) {
     using S = ScoreShape<HKV>;
-    static bool attr_set[64] = {};
-    const int dev = current_device();
-    if (dev < 0) return SV_ERR_CUDA;
-    if (dev >= 64 || !attr_set[dev]) {
-        if (cudaFuncSetAttribute(score_pages_kernel<HKV, PER_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 S::kSmemBytes) != cudaSuccess)
-            return SV_ERR_CUDA;
-        if (dev < 64) attr_set[dev] = true;
-    }
+    static std::atomic<bool> attr_set[64];
+    const int st = once_per_device(attr_set, [] {
+        return cudaFuncSetAttribute(score_pages_kernel<HKV, PER_HEAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    S::kSmemBytes) == cudaSuccess
+                   ? SV_OK
+                   : SV_ERR_CUDA;
+    });
+    if (st) return st;
     // At most one wave of one CTA per SM.  Up to SM-count requests: a
     // one-dimensional grid of X CTAs (at least 32 pages each when the
     // requests are full) that the kernel splits by the actual lengths, and

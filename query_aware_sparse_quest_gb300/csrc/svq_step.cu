@@ -862,16 +862,7 @@ __global__ void __launch_bounds__(kStepThreads, 2) quest_step_kernel(const __gri
 namespace {
 
 PFN_cuTensorMapEncodeTiled_v12000 step_tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult qr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-                cudaSuccess &&
-            qr == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encode_entry());
 }
 
 bool step_pool_map(CUtensorMap* map, const void* pool, int64_t rows) {
@@ -921,10 +912,10 @@ int launch_step_hkv(const sv_cache* c, const void* q, int num_q_heads, const int
                     const int32_t* seq_lens, int batch, int max_pages, int budget_pages, int32_t* sel_idx,
                     int32_t* sel_cnt, float softmax_scale, void* out, float* lse, void* workspace, size_t ws_bytes,
                     int sm_count, cudaStream_t stream) {
-    static int per_sm_cache[64] = {};
+    static std::atomic<int> per_sm_cache[64];
     const int dev = current_device();
     if (dev < 0) return SV_ERR_CUDA;
-    int per_sm = dev < 64 ? per_sm_cache[dev] : 0;
+    int per_sm = dev < 64 ? per_sm_cache[dev].load(std::memory_order_acquire) : 0;
     if (per_sm == 0) {
         if (cudaFuncSetAttribute(quest_step_kernel<HKV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kStepSmem) !=
             cudaSuccess)
@@ -934,7 +925,7 @@ int launch_step_hkv(const sv_cache* c, const void* q, int num_q_heads, const int
             per_sm < 1)
             return SV_ERR_CUDA;
         per_sm = min(per_sm, 2);
-        if (dev < 64) per_sm_cache[dev] = per_sm;
+        if (dev < 64) per_sm_cache[dev].store(per_sm, std::memory_order_release);
     }
     if (max_pages > kStepMaxPages) return SV_ERR_UNSUPPORTED;
     const StepLayout Ly = step_layout(batch, num_q_heads, c->num_kv_heads, max_pages, budget_pages);

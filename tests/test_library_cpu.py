@@ -17,6 +17,15 @@ HEADER = os.path.join(ROOT, "include", "svquest.h")
 SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_WORKSPACE = 0, 1, 2, 3
 
 
+# The argument-check tests below pass made-up device addresses: the checks
+# under test reject them before any launch, but if a check regressed on a
+# machine with a GPU the library would launch kernels on those addresses.
+# They therefore run only where no GPU is visible (the CPU suite), where a
+# launch cannot reach a device.
+host_only = pytest.mark.skipif(torch.cuda.is_available(),
+                               reason="fake device addresses; host-only checks run without a GPU")
+
+
 @pytest.fixture(scope="module")
 def lib():
     build.build()
@@ -70,6 +79,7 @@ def _fake_cache(page_size=16, head_dim=128, hkv=4, pages=10, null=False):
 FAKE = ctypes.c_void_p(0x20000)
 
 
+@host_only
 @pytest.mark.parametrize("cache,hq,expect", [
     (_fake_cache(null=True), 32, SV_ERR_INVALID_ARG),
     (_fake_cache(page_size=32), 32, SV_ERR_UNSUPPORTED),
@@ -84,6 +94,7 @@ def test_select_rejects_bad_geometry(lib, cache, hq, expect):
     assert st == expect
 
 
+@host_only
 def test_select_rejects_bad_sizes(lib):
     c = ctypes.byref(_fake_cache())
     assert lib.sv_quest_select(c, None, 32, FAKE, FAKE, 8, 100, 16, FAKE, FAKE, None, FAKE, 1 << 20, None) == SV_ERR_INVALID_ARG
@@ -98,12 +109,14 @@ def test_select_rejects_bad_sizes(lib):
                                1 << 20, None) == SV_ERR_INVALID_ARG
 
 
+@host_only
 def test_topk_rejects_bad_args(lib):
     assert lib.sv_quest_topk(None, FAKE, 8, 4, 100, 16, FAKE, FAKE, None) == SV_ERR_INVALID_ARG
     assert lib.sv_quest_topk(FAKE, FAKE, 8, 4, 100, 0, FAKE, FAKE, None) == SV_ERR_INVALID_ARG
     assert lib.sv_quest_topk(FAKE, FAKE, 8, 4, 32769, 16, FAKE, FAKE, None) == SV_ERR_UNSUPPORTED
 
 
+@host_only
 def test_decode_rejects_bad_args(lib):
     c = ctypes.byref(_fake_cache())
     ok = dict(q=FAKE, pt=FAKE, sl=FAKE, out=FAKE, lse=FAKE, ws=FAKE)
@@ -120,6 +133,7 @@ def test_decode_rejects_bad_args(lib):
     assert call(hq=33) == SV_ERR_INVALID_ARG
 
 
+@host_only
 def test_update_meta_rejects_bad_args(lib):
     c = ctypes.byref(_fake_cache())
     assert lib.sv_quest_update_meta(c, FAKE, FAKE, FAKE, -1, None) == SV_ERR_INVALID_ARG
@@ -142,6 +156,7 @@ def test_decode_step_workspace_size(lib):
     assert f(8, 32, 4, 100, 0) == 0
 
 
+@host_only
 def test_decode_step_rejects_bad_args(lib):
     c = ctypes.byref(_fake_cache())
 
@@ -167,6 +182,7 @@ def test_decode_step_rejects_bad_args(lib):
     assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
 
 
+@host_only
 def test_single_launch_step_limits(lib):
     def call(cache, max_pages=100):
         ws = binding.sv_quest_decode_step_workspace_size(8, 32, 4, max_pages, 16)
@@ -178,6 +194,7 @@ def test_single_launch_step_limits(lib):
     assert call(ctypes.byref(c8)) == SV_ERR_UNSUPPORTED                              # bf16 pools only
 
 
+@host_only
 def test_select_ex_and_decode_ex_option_checks(lib):
     c = ctypes.byref(_fake_cache())
 
@@ -206,6 +223,7 @@ def test_select_ex_and_decode_ex_option_checks(lib):
     assert binding.sv_quest_select_ex_workspace_size(8, 32, 4, 100, None) == 8 * 4 * 100 * 4
 
 
+@host_only
 def test_fp8_cache_checks(lib):
     def cache(fmt, ks=0x10000, vs=0x10000):
         c = _fake_cache()

@@ -75,10 +75,12 @@ def test_static_scratch_rejects_oversized_problems(cuda_ok):
     # batch 32 x 32 query heads over 8192 pages needs 64 splits of partials: 34 MB > 16 MiB.
     need = binding.sv_sparse_decode_workspace_size(32, 32, 4, 8192)
     assert need > 16 << 20
-    fake = ctypes.c_void_p(0x10000)
-    cache = binding.sv_cache(0x10000, 0x10000, 0x10000, 1000, 4, 16, 128)
-    st = lib.sv_sparse_decode_static_scratch(ctypes.byref(cache), fake, 32, fake, fake, 32, 8192, None, None, 0,
-                                             0.088, fake, fake, None)
+    # Null pools and buffers: the size check comes first and returns
+    # SV_ERR_WORKSPACE; were it ever skipped, the decode's own argument checks
+    # would return SV_ERR_INVALID_ARG (1) on the nulls, so nothing can launch.
+    cache = binding.sv_cache(None, None, None, 1000, 4, 16, 128)
+    st = lib.sv_sparse_decode_static_scratch(ctypes.byref(cache), None, 32, None, None, 32, 8192, None, None, 0,
+                                             0.088, None, None, None)
     assert st == 3    # SV_ERR_WORKSPACE, nothing launched
     # The largest batch-32 sparse problem that fits (248 pages) is accepted by the size check.
     assert binding.sv_sparse_decode_workspace_size(32, 32, 4, 248) <= 16 << 20
