@@ -10,6 +10,7 @@ passage it follows.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -20,26 +21,49 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "quest_oracle.c")
 _LIB_PATH = os.path.join(_HERE, "_build", "libquest_oracle.so")
-_lib = None
+_OMP_LIB_PATH = os.path.join(_HERE, "_build", "libquest_oracle_omp.so")
+_libs = {}
+_openmp = False
 
 
-def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (no fast-math, no FMA contraction)."""
-    if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
-        return _LIB_PATH
-    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
-    tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                    "-fno-fast-math", "-o", tmp, _SRC, "-lm"], check=True)
-    os.replace(tmp, _LIB_PATH)
-    return _LIB_PATH
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile the oracle with gcc (no fast-math, no FMA contraction).  With
+    openmp, a second library of the same source whose row loops run on the
+    host's threads (-fopenmp); the arithmetic of each row is unchanged."""
+    path = _OMP_LIB_PATH if openmp else _LIB_PATH
+    if (not force and os.path.exists(path)
+            and os.path.getmtime(path) >= os.path.getmtime(_SRC)):
+        return path
+    os.makedirs(os.path.dirname(path), exist_ok=True)
+    tmp = path + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+                    *(["-fopenmp"] if openmp else []), "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, path)
+    return path
+
+
+@contextlib.contextmanager
+def parallel():
+    """Inside the block, select and decode run on the OpenMP build: their
+    independent rows (request, head) are spread over the host's threads."""
+    global _openmp
+    prev, _openmp = _openmp, True
+    try:
+        yield num_threads()
+    finally:
+        _openmp = prev
+
+
+def num_threads() -> int:
+    """Threads the current build's row loops use (1 for the plain build)."""
+    return int(_load().oracle_num_threads())
 
 
 def _load():
-    global _lib
-    if _lib is None:
-        lib = ctypes.CDLL(build())
+    variant = _openmp
+    lib = _libs.get(variant)
+    if lib is None:
+        lib = ctypes.CDLL(build(openmp=variant))
         P = ctypes.c_void_p
         i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
         lib.oracle_update_meta.argtypes = [P, P, P, i64, i32, i32, i32, P, P, P, i64]
@@ -57,11 +81,13 @@ def _load():
         lib.oracle_e4m3_value.restype = f32
         lib.oracle_e4m3_encode.argtypes = [f32]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_num_threads.argtypes = []
         for f in (lib.oracle_update_meta, lib.oracle_select, lib.oracle_decode, lib.oracle_select_ex,
-                  lib.oracle_decode_ex, lib.oracle_quantize_rows, lib.oracle_decode_fp8, lib.oracle_topk):
+                  lib.oracle_decode_ex, lib.oracle_quantize_rows, lib.oracle_decode_fp8, lib.oracle_topk,
+                  lib.oracle_num_threads):
             f.restype = ctypes.c_int
-        _lib = lib
-    return _lib
+        _libs[variant] = lib
+    return lib
 
 
 def _ptr(a: Optional[np.ndarray]):

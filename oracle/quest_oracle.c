@@ -54,6 +54,19 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the row loops below may use: OpenMP's count in a -fopenmp build,
+ * else 1. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 static float bf16_bits_to_float(uint16_t b) {
     uint32_t u = ((uint32_t)b) << 16;
@@ -169,6 +182,45 @@ static int by_int_ascending(const void* pa, const void* pb) {
  * their logical indices ascending.  R = per_q_head ? Hq : Hkv rows.
  * scores (nullable) receives [B][R][max_pages] fp32 (the bound, also for
  * forced pages), entries past n_b untouched.
+ *
+ * select_row computes one row (request b, row r); `list` holds max_pages
+ * entries of scratch.
+ */
+static int select_row(const uint16_t* q, const uint16_t* meta, const int32_t* page_table,
+                      const int32_t* seq_lens, int Hq, int Hkv, int D, int P, int max_pages, int K,
+                      int64_t n_phys, int per_q_head, int sink_pages, int window_pages, int b, int r,
+                      scored_page* list, int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
+    const int G = Hq / Hkv;
+    const int R = per_q_head ? Hq : Hkv;
+    int n = (seq_lens[b] + P - 1) / P;
+    if (n < 1 || n > max_pages) return -2;
+    const int g = per_q_head ? r / G : r;
+    const int first_head = per_q_head ? r : g * G;
+    const int heads = per_q_head ? 1 : G;
+    const uint16_t* qr = q + ((size_t)b * Hq + (size_t)first_head) * D;
+    for (int p = 0; p < n; ++p) {
+        int64_t phys = page_table[(size_t)b * max_pages + p];
+        if (phys < 0 || phys >= n_phys) return -2;
+        const uint16_t* kmin = meta + (((size_t)phys * Hkv + g) * 2 + 0) * D;
+        const uint16_t* kmax = meta + (((size_t)phys * Hkv + g) * 2 + 1) * D;
+        list[p].score = page_bound(qr, heads, D, kmin, kmax);
+        list[p].page = p;
+        list[p].forced = (p < sink_pages || p >= n - window_pages) ? 1 : 0;
+        if (scores) scores[((size_t)b * R + r) * max_pages + p] = list[p].score;
+    }
+    qsort(list, (size_t)n, sizeof(scored_page), by_score_then_index);
+    int m = n < K ? n : K;
+    int32_t* out = sel_idx + ((size_t)b * R + r) * K;
+    for (int j = 0; j < m; ++j) out[j] = list[j].page;
+    qsort(out, (size_t)m, sizeof(int32_t), by_int_ascending);
+    for (int j = m; j < K; ++j) out[j] = -1;
+    sel_cnt[(size_t)b * R + r] = m;
+    return 0;
+}
+
+/* Rows are independent: a build with OpenMP (-fopenmp) hands them to the
+ * host's threads, each with its own scratch; without it the loop runs in
+ * order on one thread.  Either way every row is computed by select_row alone.
  */
 int oracle_select_ex(const uint16_t* q, const uint16_t* meta,
                      const int32_t* page_table, const int32_t* seq_lens,
@@ -176,39 +228,26 @@ int oracle_select_ex(const uint16_t* q, const uint16_t* meta,
                      int64_t n_phys, int per_q_head, int sink_pages, int window_pages,
                      int32_t* sel_idx, int32_t* sel_cnt, float* scores) {
     if (Hq % Hkv != 0 || K < 1 || sink_pages < 0 || window_pages < 0) return -1;
-    const int G = Hq / Hkv;
     const int R = per_q_head ? Hq : Hkv;
-    scored_page* list = (scored_page*)malloc((size_t)max_pages * sizeof(scored_page));
-    if (!list) return -1;
-    for (int b = 0; b < B; ++b) {
-        int n = (seq_lens[b] + P - 1) / P;
-        if (n < 1 || n > max_pages) { free(list); return -2; }
-        for (int r = 0; r < R; ++r) {
-            const int g = per_q_head ? r / G : r;
-            const int first_head = per_q_head ? r : g * G;
-            const int heads = per_q_head ? 1 : G;
-            const uint16_t* qr = q + ((size_t)b * Hq + (size_t)first_head) * D;
-            for (int p = 0; p < n; ++p) {
-                int64_t phys = page_table[(size_t)b * max_pages + p];
-                if (phys < 0 || phys >= n_phys) { free(list); return -2; }
-                const uint16_t* kmin = meta + (((size_t)phys * Hkv + g) * 2 + 0) * D;
-                const uint16_t* kmax = meta + (((size_t)phys * Hkv + g) * 2 + 1) * D;
-                list[p].score = page_bound(qr, heads, D, kmin, kmax);
-                list[p].page = p;
-                list[p].forced = (p < sink_pages || p >= n - window_pages) ? 1 : 0;
-                if (scores) scores[((size_t)b * R + r) * max_pages + p] = list[p].score;
+    const int64_t rows = (int64_t)B * R;
+    int rc = 0;
+#pragma omp parallel
+    {
+        scored_page* list = (scored_page*)malloc((size_t)max_pages * sizeof(scored_page));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t row = 0; row < rows; ++row) {
+            int e = list ? select_row(q, meta, page_table, seq_lens, Hq, Hkv, D, P, max_pages, K, n_phys,
+                                      per_q_head, sink_pages, window_pages, (int)(row / R), (int)(row % R), list,
+                                      sel_idx, sel_cnt, scores)
+                         : -1;
+            if (e) {
+#pragma omp atomic write
+                rc = e;
             }
-            qsort(list, (size_t)n, sizeof(scored_page), by_score_then_index);
-            int m = n < K ? n : K;
-            int32_t* out = sel_idx + ((size_t)b * R + r) * K;
-            for (int j = 0; j < m; ++j) out[j] = list[j].page;
-            qsort(out, (size_t)m, sizeof(int32_t), by_int_ascending);
-            for (int j = m; j < K; ++j) out[j] = -1;
-            sel_cnt[(size_t)b * R + r] = m;
         }
+        free(list);
     }
-    free(list);
-    return 0;
+    return rc;
 }
 
 /*
@@ -261,72 +300,104 @@ int oracle_select(const uint16_t* q, const uint16_t* meta,
  *   out = sum exp(z_t - m) v_t / l;  lse = m + ln(l).
  * out is fp32 [B][Hq][D]; lse fp32 [B][Hq].
  */
+/* One query head (request b, head h) of oracle_decode_ex; z, tok_page and
+ * tok_off hold max_pages * P entries of scratch. */
+static int decode_head(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
+                       const int32_t* page_table, const int32_t* seq_lens, int Hq, int Hkv, int D, int P,
+                       int max_pages, int64_t n_phys, const int32_t* sel_idx, const int32_t* sel_cnt, int K,
+                       int per_q_head, float scale, int b, int h, float* z, int32_t* tok_page, int32_t* tok_off,
+                       float* out, float* lse) {
+    const int G = Hq / Hkv;
+    const int R = per_q_head ? Hq : Hkv;
+    int len = seq_lens[b];
+    int n = (len + P - 1) / P;
+    if (n < 1 || n > max_pages) return -2;
+    int g = h / G;
+    int r = per_q_head ? h : g;
+    int count = sel_idx ? sel_cnt[(size_t)b * R + r] : n;
+    if (count < 0 || count > (sel_idx ? K : n)) return -2;
+    /* Gather the attended tokens as (physical page, offset). */
+    int ntok = 0;
+    for (int j = 0; j < count; ++j) {
+        int p = sel_idx ? sel_idx[((size_t)b * R + r) * K + j] : j;
+        if (p < 0 || p >= n) return -2;
+        int64_t phys = page_table[(size_t)b * max_pages + p];
+        if (phys < 0 || phys >= n_phys) return -2;
+        int valid = (p == n - 1) ? len - P * (n - 1) : P;
+        for (int o = 0; o < valid; ++o) {
+            tok_page[ntok] = (int32_t)phys;
+            tok_off[ntok] = o;
+            ++ntok;
+        }
+    }
+    const uint16_t* qh = q + ((size_t)b * Hq + h) * D;
+    float* o_row = out + ((size_t)b * Hq + h) * D;
+    float m = -INFINITY;
+    for (int t = 0; t < ntok; ++t) {
+        const uint16_t* k = k_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
+        float dot = 0.0f;
+        for (int i = 0; i < D; ++i) dot += bf16_bits_to_float(qh[i]) * bf16_bits_to_float(k[i]);
+        z[t] = dot * scale;
+        if (z[t] > m) m = z[t];
+    }
+    float l = 0.0f;
+    for (int i = 0; i < D; ++i) o_row[i] = 0.0f;
+    for (int t = 0; t < ntok; ++t) {
+        float w = expf(z[t] - m);
+        l += w;
+        const uint16_t* v = v_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
+        for (int i = 0; i < D; ++i) o_row[i] += w * bf16_bits_to_float(v[i]);
+    }
+    if (ntok == 0) {
+        lse[(size_t)b * Hq + h] = -INFINITY;
+        return 0;
+    }
+    for (int i = 0; i < D; ++i) o_row[i] /= l;
+    lse[(size_t)b * Hq + h] = m + logf(l);
+    return 0;
+}
+
+/*
+ * Exact softmax attention of every query head over the tokens of a page
+ * list: all n_b logical pages when sel_idx is NULL (dense), else the
+ * sel_cnt[b][r] pages of sel_idx[b][r], r = the head's kv group g, or the
+ * head itself when per_q_head (sel_idx then has Hq rows per request).  The last logical page n_b - 1 holds
+ * len_b - P*(n_b - 1) tokens; every other page holds P.
+ *   z_t = (q . k_t) * scale;  m = max z;  l = sum exp(z - m);
+ *   out = sum exp(z_t - m) v_t / l;  lse = m + ln(l).
+ * out is fp32 [B][Hq][D]; lse fp32 [B][Hq].  Heads are independent: an
+ * OpenMP build hands them to the host's threads (each with its own scratch),
+ * a plain build runs them in order; each head is computed by decode_head alone.
+ */
 int oracle_decode_ex(const uint16_t* q, const uint16_t* k_pool, const uint16_t* v_pool,
                      const int32_t* page_table, const int32_t* seq_lens,
                      int B, int Hq, int Hkv, int D, int P, int max_pages, int64_t n_phys,
                      const int32_t* sel_idx, const int32_t* sel_cnt, int K, int per_q_head, float scale,
                      float* out, float* lse) {
     if (Hq % Hkv != 0) return -1;
-    const int G = Hq / Hkv;
-    const int R = per_q_head ? Hq : Hkv;
-    float* z = (float*)malloc((size_t)max_pages * P * sizeof(float));
-    int32_t* tok_page = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
-    int32_t* tok_off = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
-    if (!z || !tok_page || !tok_off) { free(z); free(tok_page); free(tok_off); return -1; }
+    const int64_t heads = (int64_t)B * Hq;
     int rc = 0;
-    for (int b = 0; b < B && rc == 0; ++b) {
-        int len = seq_lens[b];
-        int n = (len + P - 1) / P;
-        if (n < 1 || n > max_pages) { rc = -2; break; }
-        for (int h = 0; h < Hq && rc == 0; ++h) {
-            int g = h / G;
-            int r = per_q_head ? h : g;
-            int count = sel_idx ? sel_cnt[(size_t)b * R + r] : n;
-            if (count < 0 || count > (sel_idx ? K : n)) { rc = -2; break; }
-            /* Gather the attended tokens as (physical page, offset). */
-            int ntok = 0;
-            for (int j = 0; j < count; ++j) {
-                int p = sel_idx ? sel_idx[((size_t)b * R + r) * K + j] : j;
-                if (p < 0 || p >= n) { rc = -2; break; }
-                int64_t phys = page_table[(size_t)b * max_pages + p];
-                if (phys < 0 || phys >= n_phys) { rc = -2; break; }
-                int valid = (p == n - 1) ? len - P * (n - 1) : P;
-                for (int o = 0; o < valid; ++o) {
-                    tok_page[ntok] = (int32_t)phys;
-                    tok_off[ntok] = o;
-                    ++ntok;
-                }
+#pragma omp parallel
+    {
+        float* z = (float*)malloc((size_t)max_pages * P * sizeof(float));
+        int32_t* tok_page = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
+        int32_t* tok_off = (int32_t*)malloc((size_t)max_pages * P * sizeof(int32_t));
+        const int ok = z && tok_page && tok_off;
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t bh = 0; bh < heads; ++bh) {
+            int e = ok ? decode_head(q, k_pool, v_pool, page_table, seq_lens, Hq, Hkv, D, P, max_pages, n_phys,
+                                     sel_idx, sel_cnt, K, per_q_head, scale, (int)(bh / Hq), (int)(bh % Hq), z,
+                                     tok_page, tok_off, out, lse)
+                       : -1;
+            if (e) {
+#pragma omp atomic write
+                rc = e;
             }
-            if (rc) break;
-            const uint16_t* qh = q + ((size_t)b * Hq + h) * D;
-            float* o_row = out + ((size_t)b * Hq + h) * D;
-            float m = -INFINITY;
-            for (int t = 0; t < ntok; ++t) {
-                const uint16_t* k = k_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
-                float dot = 0.0f;
-                for (int i = 0; i < D; ++i) dot += bf16_bits_to_float(qh[i]) * bf16_bits_to_float(k[i]);
-                z[t] = dot * scale;
-                if (z[t] > m) m = z[t];
-            }
-            float l = 0.0f;
-            for (int i = 0; i < D; ++i) o_row[i] = 0.0f;
-            for (int t = 0; t < ntok; ++t) {
-                float w = expf(z[t] - m);
-                l += w;
-                const uint16_t* v = v_pool + (((size_t)tok_page[t] * Hkv + g) * P + tok_off[t]) * D;
-                for (int i = 0; i < D; ++i) o_row[i] += w * bf16_bits_to_float(v[i]);
-            }
-            if (ntok == 0) {
-                lse[(size_t)b * Hq + h] = -INFINITY;
-                continue;
-            }
-            for (int i = 0; i < D; ++i) o_row[i] /= l;
-            lse[(size_t)b * Hq + h] = m + logf(l);
         }
+        free(z);
+        free(tok_page);
+        free(tok_off);
     }
-    free(z);
-    free(tok_page);
-    free(tok_off);
     return rc;
 }
 

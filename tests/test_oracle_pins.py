@@ -528,3 +528,31 @@ def test_fp8_rows_and_attention():
             o_ref, l_ref = _sdpa_fp64(qf[b, h : h + 1], k, v, 0.3)
             np.testing.assert_allclose(out[b, h], o_ref[0], rtol=2e-5, atol=2e-6)
             np.testing.assert_allclose(lse[b, h], l_ref[0], rtol=2e-6, atol=2e-6)
+
+
+def test_openmp_build_matches_the_plain_build_bit_for_bit():
+    """The OpenMP build only hands independent rows (request, head) to the
+    host's threads: selections, scores, outputs and lse equal the plain
+    build's bit for bit, on a ragged batch with partial last pages, dense and
+    sparse, group and per-query-head rows."""
+    wl = synth.make_workload(synth.SPECS[3].scaled(batch=5, ragged=(16 * 30 + 3, 16 * 90 + 11),
+                                                   budget_pages=12))
+    host = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    args = (host, wl.q, wl.page_table, wl.seq_lens)
+
+    def run():
+        res = []
+        for per_head in (False, True):
+            sel, cnt, sc = oracle.select(*args, wl.spec.budget_pages, per_q_head=per_head)
+            res += [sel, cnt, sc, *oracle.decode(*args, sel, cnt, per_q_head=per_head)]
+        res += list(oracle.decode(*args))
+        return res
+
+    plain = run()
+    with oracle.parallel() as threads:
+        assert threads >= 1
+        par = run()
+    assert oracle.num_threads() == 1
+    for a, b in zip(plain, par):
+        assert a.dtype == b.dtype and a.shape == b.shape
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
