@@ -169,11 +169,10 @@ def algorithmic_bytes(wl):
 
 # Kernels each public call launches (include/svquest.h): sv_quest_score and
 # sv_quest_topk one each, sv_sparse_decode two (split-K flash decode, then the
-# log-sum-exp combine), sv_quest_decode_step the same four, the single-launch
-# step one cooperative kernel (after a memset of its counters),
-# sv_quest_update_meta one.
+# log-sum-exp combine), sv_quest_decode_step four (scores, top-K, split-K
+# decode, combine), sv_quest_update_meta one.
 KERNELS_PER_CALL = {"sv_quest_score": 1, "sv_quest_topk": 1, "sv_sparse_decode": 2, "sv_quest_decode_step": 4,
-                    "sv_quest_decode_step_single_launch": 1, "sv_quest_update_meta": 1}
+                    "sv_quest_update_meta": 1}
 STEP_CALLS = ("sv_quest_decode_step",)
 
 
@@ -306,20 +305,8 @@ def run_gpu(args):
     # ---- dense (all pages) comparator
     dense_ms = float(np.mean(timed(g_dense.replay, max(3, min(args.steps, 50)))))
 
-    # ---- the same step as one cooperative launch (sv_quest_decode_step_single_launch)
-    sel2, cnt2 = resident.select_buffers(B, Hkv, K, dev)
-    out2, lse2 = torch.empty_like(out), torch.empty_like(lse)
-    ws_single = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, max_pages, K), dev)
-
-    def fused():
-        binding.sv_quest_decode_step_single_launch(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel2, cnt2, out2,
-                                                   lse2, ws_single)
-
-    fused()
     step()   # the step again (the dense comparator overwrote out / lse)
     torch.cuda.synchronize(dev)
-    fused_agree = bool(torch.equal(cnt2, sel_cnt)) and float((out2.float() - out.float()).abs().max()) <= 2e-2
-    fused_ms = float(np.mean(timed(fused, max(3, min(args.steps, 200)))))
 
     # ---- bulk prefill append: one 4096-token chunk through sv_quest_update_meta
     # (request 0's first 4096 tokens rewritten into their own slots: same pool)
@@ -453,10 +440,6 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "how": e2e_how,
                 "eager_ms_per_step": round(e2e_eager_ms, 5), "result_copied_back": e2e_ok},
-        "fused_step": {"ms_per_step": round(fused_ms, 5), "steps_per_s": round(1e3 / fused_ms, 2),
-                       "agrees_with_step": fused_agree,
-                       "note": "sv_quest_decode_step_single_launch: the same step as one cooperative launch, "
-                               "timed alone"},
         "fp8_step": {"ms_per_step": round(fp8_ms, 5), "steps_per_s": round(1e3 / fp8_ms, 2),
                      "bytes": ab["fp8_step"], "gbs": round(ab["fp8_step"] / (fp8_ms * 1e-3) / 1e9, 1),
                      "sparse_decode_ms": round(fp8_dec_ms, 5),
@@ -568,14 +551,6 @@ def run_all_configs(args):
             entry = {"budget_pages": K, "us": round(ms * 1e3, 2), "steps_per_s": round(1e3 / ms, 1),
                      "bytes": nb, "gbs": round(nb / (ms * 1e-3) / 1e9, 1),
                      "frac_of_measured": round(nb / (ms * 1e-3) / 1e9 / peak, 4)}
-            if wl.max_pages <= 8192:
-                def single(K=K, sel=sel, cnt=cnt, ws=ws):
-                    if pre is not None:
-                        pre()
-                    binding.sv_quest_decode_step_single_launch(dw.cache, q, dw.page_table, dw.seq_lens, K, sel, cnt,
-                                                               out, lse, ws)
-
-                entry["single_launch_us"] = round(timed(graph_of(single).replay, n_timed, n_warm) * 1e3, 2)
             steps.append(entry)
             del sel, cnt, ws
         wsd = resident.workspace(binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, wl.max_pages), dev)

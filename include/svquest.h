@@ -62,7 +62,8 @@ enum sv_status {
 #define SV_DEVERR_SEL_IDX    0x2u   /* sel_idx entry outside [0, n_b) or sel_cnt out of range */
 #define SV_DEVERR_SLOT       0x4u   /* slot_mapping entry outside the pool */
 #define SV_DEVERR_SEQ_LEN    0x8u   /* seq_lens[b] < 1 or needs more than max_pages pages */
-#define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up waiting for its own bulk copies */
+#define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up a wait (its own bulk copies, or an earlier
+                                       kernel's request or row flag) after 2^28 SM clock cycles */
 
 /* K/V pool formats (sv_cache.kv_format). */
 #define SV_KV_BF16     0   /* k_pool, v_pool bf16 [pages][Hkv][16][128] */
@@ -80,7 +81,7 @@ enum sv_status {
  * back as value(code) * s.  The metadata stays bf16 and holds the min / max
  * of the keys as appended (before coding), so page selection is the same as
  * for bf16 pools; only attention reads the coded rows.  All calls accept both
- * formats except sv_quest_decode_step_single_launch (bf16 only).
+ * formats.
  */
 typedef struct sv_cache {
     void* k_pool;             /* [num_phys_pages][num_kv_heads][16][128] of the format's element */
@@ -264,13 +265,26 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
  * the view (exactly sv_sparse_decode), the decode-time hooks of the
  * SparseEngine page ("method key points": query-relevant page selection
  * before attention, then attention over the selected pages only).  It
- * enqueues the same four kernels back to back with programmatic dependent
- * launch.
+ * enqueues four kernels back to back with programmatic dependent launch:
+ * page scores, top-K, split-K attention, log-sum-exp combine.
  *  - budget_pages >= 1 is the row length of sel_idx, as in sv_quest_select.
  *  - softmax_scale > 0, as in sv_sparse_decode.
  *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
  *    with a call that may run at the same time; nothing in it needs to start
  *    at zero.
+ *  - Pipelining (a build option; batch * num_kv_heads <= 32 and
+ *    max_pages <= 16384): the scoring kernel then scores the batch request
+ *    after request, and a few
+ *    words at the end of the workspace let each request's top-K start as
+ *    soon as that request is scored and each (request, kv head) row's
+ *    attention as soon as its selection is written, instead of each kernel
+ *    waiting for the whole previous one.  The first call on a workspace (or
+ *    the first after a call of another geometry) runs whole kernel after
+ *    whole kernel; every call ends by resetting those words and marking them
+ *    for its geometry, which lets the next call on the same workspace run
+ *    pipelined.  Results are the same either way.  After a call that
+ *    reported SV_DEVERR_TIMEOUT, zero the workspace (or use another one)
+ *    before the next call.
  */
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
                          const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
@@ -278,28 +292,7 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
                          int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
                          void* workspace, size_t workspace_bytes, void* stream);
 
-/*
- * sv_quest_decode_step_single_launch -- the same step as ONE persistent
- * cooperative kernel (scoring, top-K, split attention and combine scheduled
- * inside the launch; the pages prescribe no fusion).  Results: sel_idx /
- * sel_cnt identical to sv_quest_decode_step's up to page scores that differ
- * only in fp32 rounding order, out / lse equal up to the split-K summation
- * order.  Arguments and workspace as sv_quest_decode_step (the call clears its
- * own counters first).  bf16 pools with max_pages <= 8192 (131072 tokens)
- * only, else SV_ERR_UNSUPPORTED.  Every CTA must be co-resident: the call
- * returns SV_ERR_CUDA if the device cannot hold the grid (e.g. another
- * context holds its SMs under MPS).  It is slower than sv_quest_decode_step
- * (on GB300, 8 requests of 128000 tokens: about 92 us against 52 us): its
- * scoring CTAs share each SM's shared memory with attention stages, so fewer
- * metadata bytes are in flight.  It serves callers that need one launch.
- */
-int sv_quest_decode_step_single_launch(const sv_cache* cache, const void* q, int32_t num_q_heads,
-                                       const int32_t* page_table, const int32_t* seq_lens, int32_t batch,
-                                       int32_t max_pages, int32_t budget_pages, float softmax_scale,
-                                       int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
-                                       void* workspace, size_t workspace_bytes, void* stream);
-
-/* Enough workspace for both step calls. */
+/* Workspace bytes of sv_quest_decode_step. */
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t max_pages, int32_t budget_pages);
 

@@ -64,7 +64,6 @@ def _load():
         "sv_sparse_decode": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp, sz, vp],
         "sv_sparse_decode_static_scratch": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, f32, vp, vp, vp],
         "sv_quest_decode_step": [cp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
-        "sv_quest_decode_step_single_launch": [cp, vp, i32, vp, vp, i32, i32, i32, f32, vp, vp, vp, vp, vp, sz, vp],
         "sv_quest_select_ex": [cp, vp, i32, vp, vp, i32, i32, i32, op, vp, vp, vp, vp, sz, vp],
         "sv_sparse_decode_ex": [cp, vp, i32, vp, vp, i32, i32, vp, vp, i32, op, f32, vp, vp, vp, sz, vp],
         "sv_get_device_error": [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int],
@@ -227,15 +226,6 @@ def sv_quest_decode_step(cache: Cache, q: torch.Tensor, page_table: torch.Tensor
                          stream=None) -> None:
     _step("sv_quest_decode_step", cache, q, page_table, seq_lens, budget_pages, sel_idx, sel_cnt, out, lse,
           workspace, softmax_scale, stream)
-
-
-def sv_quest_decode_step_single_launch(cache: Cache, q: torch.Tensor, page_table: torch.Tensor,
-                                       seq_lens: torch.Tensor, budget_pages: int, sel_idx: torch.Tensor,
-                                       sel_cnt: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
-                                       workspace: torch.Tensor, softmax_scale: Optional[float] = None,
-                                       stream=None) -> None:
-    _step("sv_quest_decode_step_single_launch", cache, q, page_table, seq_lens, budget_pages, sel_idx, sel_cnt, out,
-          lse, workspace, softmax_scale, stream)
 
 
 def quest_opts(per_q_head: bool = False, sink_pages: int = 0, window_pages: int = 0, layer: int = 0,

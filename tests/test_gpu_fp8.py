@@ -140,10 +140,6 @@ def test_fp8_decode_step_and_error_vs_bf16():
     ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, spec.num_kv_heads,
                                                                         dw.page_table.shape[1], K))
     binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse, ws)
-    with pytest.raises(binding.SvError) as e:   # the single launch is bf16-only
-        binding.sv_quest_decode_step_single_launch(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx,
-                                                   sel_cnt, out, lse, ws)
-    assert e.value.status == 2
     sel, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
     o8, l8 = out.float().cpu().numpy(), lse.cpu().numpy()
     check_attention(o8, l8, *oracle.decode(host, wl.q, wl.page_table, wl.seq_lens, sel, cnt))
@@ -154,3 +150,34 @@ def test_fp8_decode_step_and_error_vs_bf16():
     # A statistic of the codec (per-row scales meet outlier key channels), not a
     # parity bar; the bound only catches a gross error such as a lost scale.
     assert diff.max() < 1.0
+
+
+def test_fp8_step_full_size_128k():
+    """The benchmark's workload (8 requests of 128000 tokens, budget 256
+    pages, shuffled 64000-page pool) on an fp8 pool through
+    sv_quest_decode_step, twice on one workspace (the first call whole kernel
+    after whole kernel, the second pipelined): every selection against the
+    oracle, attention of two sampled requests against the oracle's fp8
+    decode over those selections, and the two calls bitwise equal."""
+    wl, dw, host = _pair(synth.SPECS[2])
+    spec = wl.spec
+    K = spec.budget_pages
+    B, Hq, D = dw.q.shape
+    ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, spec.num_kv_heads, wl.max_pages, K))
+    runs = []
+    for _ in range(2):
+        sel_idx, sel_cnt = resident.select_buffers(B, spec.num_kv_heads, K)
+        out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse, ws)
+        runs.append((sel_idx.cpu().numpy(), sel_cnt.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()))
+    for a, b in zip(*runs):
+        assert np.array_equal(a, b, equal_nan=True)
+    sel, cnt, out, lse = runs[1]
+    ref_sel, ref_cnt, ref_scores = oracle.select(host, wl.q, wl.page_table, wl.seq_lens, K)
+    check_selection(sel, cnt, ref_sel, ref_cnt, ref_scores, n_pages_of(wl))
+    for b in (0, 5):
+        rows = slice(b, b + 1)
+        ref_out, ref_lse = oracle.decode(host, wl.q[rows], wl.page_table[rows], wl.seq_lens[rows], sel[rows],
+                                         cnt[rows])
+        check_attention(out[rows], lse[rows], ref_out, ref_lse)

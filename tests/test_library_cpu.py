@@ -145,13 +145,13 @@ def test_update_meta_rejects_bad_args(lib):
 
 def test_decode_step_workspace_size(lib):
     f = binding.sv_quest_decode_step_workspace_size
-    # fused path: scores + split-K partials (16 pages per split, <= 64 splits) + counters
-    ws = f(8, 32, 4, 8000, 256)
-    assert ws >= 8 * 4 * 8000 * 4 + 8 * 32 * 16 * (128 * 4 + 8) + (1 + 8 + 2 * 32) * 4
+    # select scores + sparse-decode partials + the pipelined step's words
+    # (a 2-word header, one count per request, one flag per (request, kv head))
+    for args in ((8, 32, 4, 8000, 256), (2, 8, 1, 9000, 64), (32, 32, 4, 8192, 128)):
+        B, Hq, Hkv, mp, K = args
+        assert f(*args) >= (binding.sv_quest_select_workspace_size(B, Hkv, mp)
+                            + binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, K) + (2 + B + B * Hkv) * 4)
     assert f(8, 32, 4, 8000, 256) < f(8, 32, 4, 8000, 512)
-    # two-stage path above 8192 pages: select scores + sparse-decode partials
-    assert f(2, 8, 1, 9000, 64) >= (binding.sv_quest_select_workspace_size(2, 1, 9000)
-                                    + binding.sv_sparse_decode_workspace_size(2, 8, 1, 64))
     assert f(0, 32, 4, 100, 16) == 0
     assert f(8, 32, 4, 100, 0) == 0
 
@@ -180,18 +180,6 @@ def test_decode_step_rejects_bad_args(lib):
     need = binding.sv_quest_decode_step_workspace_size(8, 32, 4, 100, 16)
     assert call(ws_bytes=need - 1) == SV_ERR_WORKSPACE
     assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
-
-
-@host_only
-def test_single_launch_step_limits(lib):
-    def call(cache, max_pages=100):
-        ws = binding.sv_quest_decode_step_workspace_size(8, 32, 4, max_pages, 16)
-        return lib.sv_quest_decode_step_single_launch(cache, FAKE, 32, FAKE, FAKE, 8, max_pages, 16, 0.088, FAKE,
-                                                      FAKE, FAKE, FAKE, FAKE, ws, None)
-    assert call(ctypes.byref(_fake_cache()), max_pages=9000) == SV_ERR_UNSUPPORTED   # rows above 8192 pages
-    c8 = _fake_cache()
-    c8.kv_format, c8.k_scale, c8.v_scale = binding.SV_KV_FP8_E4M3, 0x10000, 0x10000
-    assert call(ctypes.byref(c8)) == SV_ERR_UNSUPPORTED                              # bf16 pools only
 
 
 @host_only
