@@ -62,8 +62,8 @@ enum sv_status {
 #define SV_DEVERR_SEL_IDX    0x2u   /* sel_idx entry outside [0, n_b) or sel_cnt out of range */
 #define SV_DEVERR_SLOT       0x4u   /* slot_mapping entry outside the pool */
 #define SV_DEVERR_SEQ_LEN    0x8u   /* seq_lens[b] < 1 or needs more than max_pages pages */
-#define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up a wait (its own bulk copies, or an earlier
-                                       kernel's request or row flag) after 2^28 SM clock cycles */
+#define SV_DEVERR_TIMEOUT    0x10u  /* a kernel gave up a wait on its own bulk copies after
+                                       2^28 SM clock cycles */
 
 /* K/V pool formats (sv_cache.kv_format). */
 #define SV_KV_BF16     0   /* k_pool, v_pool bf16 [pages][Hkv][16][128] */
@@ -272,19 +272,6 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
  *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
  *    with a call that may run at the same time; nothing in it needs to start
  *    at zero.
- *  - Pipelining (a build option; batch * num_kv_heads <= 32 and
- *    max_pages <= 16384): the scoring kernel then scores the batch request
- *    after request, and a few
- *    words at the end of the workspace let each request's top-K start as
- *    soon as that request is scored and each (request, kv head) row's
- *    attention as soon as its selection is written, instead of each kernel
- *    waiting for the whole previous one.  The first call on a workspace (or
- *    the first after a call of another geometry) runs whole kernel after
- *    whole kernel; every call ends by resetting those words and marking them
- *    for its geometry, which lets the next call on the same workspace run
- *    pipelined.  Results are the same either way.  After a call that
- *    reported SV_DEVERR_TIMEOUT, zero the workspace (or use another one)
- *    before the next call.
  */
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
                          const int32_t* page_table, const int32_t* seq_lens, int32_t batch,

@@ -19,22 +19,12 @@ int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                   const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
-                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream,
-                  const PipeSync* ps, int pipe_words);
-int pipe_select_supported(int batch, int num_kv_heads, int max_pages, int sm_count);
-int launch_select_pipe(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
-                       const int32_t* seq_lens, int batch, int max_pages, int budget_pages, float* scores,
-                       int32_t* sel_idx, int32_t* sel_cnt, const PipeSync& ps, cudaStream_t stream);
+                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream);
 int decode_max_splits(int pages);
 size_t decode_workspace_bytes(int batch, int num_q_heads, int splits);
 int read_error_decode_fp8(uint32_t* flags, int reset);
 
 constexpr int kMaxTopkPages = 32768;
-// The pipelined step (request-major scoring, per-request top-K, per-row
-// attention); 0 runs whole kernel after whole kernel.
-#ifndef SVQ_STEP_PIPELINE
-#define SVQ_STEP_PIPELINE 0
-#endif
 
 namespace {
 
@@ -149,31 +139,9 @@ int decode_impl(const sv_cache* cache, const void* q, int32_t num_q_heads, const
     if ((st = sm_count_of_current_device(&sms))) return st;
     return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
                          budget_pages, opts->per_q_head != 0, softmax_scale, out, lse, workspace, workspace_bytes,
-                         sms, static_cast<cudaStream_t>(stream), nullptr, 0);
+                         sms, static_cast<cudaStream_t>(stream));
 }
 
-// The separate-kernel step's workspace: scores, then split-K partials, then
-// (256-byte aligned) the pipelined step's words: a 2-word header, done[batch]
-// and rowready[batch * num_kv_heads].
-size_t step_sync_offset(int batch, int num_q_heads, int num_kv_heads, int max_pages, int budget_pages) {
-    const size_t partials = decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
-    return scores_bytes(batch, num_kv_heads, max_pages) + (partials + 255) / 256 * 256;
-}
-size_t step_sync_bytes(int batch, int num_kv_heads) {
-    return (static_cast<size_t>(2 + batch + batch * num_kv_heads) * 4 + 255) / 256 * 256;
-}
-// Distinguishes the geometries that may share a workspace: a header armed by
-// a step of another geometry (or never armed) is not this step's.
-uint32_t step_sync_key(int batch, int num_kv_heads, int score_ctas, size_t sync_offset) {
-    uint32_t k = 0x2545F491u;
-    const uint64_t parts[4] = {static_cast<uint64_t>(batch), static_cast<uint64_t>(num_kv_heads),
-                               static_cast<uint64_t>(score_ctas), static_cast<uint64_t>(sync_offset)};
-    for (uint64_t v : parts) {
-        k ^= static_cast<uint32_t>(v) + 0x9E3779B9u + (k << 6) + (k >> 2);
-        k ^= static_cast<uint32_t>(v >> 32) * 0x85EBCA6Bu;
-    }
-    return k == kPipeMagic ? k + 1u : k;
-}
 
 }  // namespace
 }  // namespace svq
@@ -269,9 +237,9 @@ int sv_sparse_decode_ex(const sv_cache* cache, const void* q, int32_t num_q_head
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t max_pages, int32_t budget_pages) {
     if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_pages < 1 || budget_pages < 1) return 0;
-    // Scores, split-K partials, the pipelined step's synchronisation words.
-    return step_sync_offset(batch, num_q_heads, num_kv_heads, max_pages, budget_pages) +
-           step_sync_bytes(batch, num_kv_heads);
+    // Scores at the front, split-K partials after.
+    return scores_bytes(batch, num_kv_heads, max_pages) +
+           decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
 }
 
 }  // extern "C"
@@ -309,37 +277,17 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Scores at the front of the workspace, split-K partials after, then the
-    // pipelined step's synchronisation words.
+    // Scores at the front of the workspace, split-K partials after.
     const int hkv = cache->num_kv_heads;
     const size_t sb = scores_bytes(batch, hkv, max_pages);
-    const size_t sync_off = step_sync_offset(batch, num_q_heads, hkv, max_pages, budget_pages);
     float* scores = static_cast<float*>(workspace);
-    unsigned char* ws = static_cast<unsigned char*>(workspace);
-    if (SVQ_STEP_PIPELINE && pipe_select_supported(batch, hkv, max_pages, sms)) {
-        // Pipelined: request-major scoring, top-K per request as soon as it is
-        // scored, attention per row as soon as it is selected (flags in the
-        // workspace; the first step on a workspace runs as the classic chain
-        // and arms it for the next).
-        PipeSync ps;
-        ps.header = reinterpret_cast<uint32_t*>(ws + sync_off);
-        ps.done = ps.header + 2;
-        ps.rowready = ps.done + batch;
-        ps.key = step_sync_key(batch, hkv, sms, sync_off);
-        ps.score_ctas = sms;
-        if ((st = launch_select_pipe(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, budget_pages,
-                                     scores, sel_idx, sel_cnt, ps, s)))
-            return st;
-        return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                             budget_pages, false, softmax_scale, out, lse, ws + sb, sync_off - sb, sms, s, &ps,
-                             batch + batch * hkv);
-    }
     if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s)))
         return st;
     if ((st = launch_topk(scores, seq_lens, batch, hkv, max_pages, budget_pages, sel_idx, sel_cnt, s)))
         return st;
     return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                         budget_pages, false, softmax_scale, out, lse, ws + sb, sync_off - sb, sms, s, nullptr, 0);
+                         budget_pages, false, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
+                         workspace_bytes - sb, sms, s);
 }
 
 int sv_get_device_error(uint32_t* flags, int reset) {

@@ -142,51 +142,6 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 // async-proxy (bulk copy) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// ---------------------------------------------------------------- flags between kernels of one step
-// The pipelined decode step lets a kernel start on a request (or a selection
-// row) as soon as the kernel before it has finished that request, instead of
-// waiting for its whole grid: producers publish a count or flag with release
-// semantics after their data, consumers poll it with acquire loads.  Every
-// poll loop is bounded; a loop that gives up reports SV_DEVERR_TIMEOUT.
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-constexpr uint32_t kFlagPollLimit = 1u << 22;
-__device__ __forceinline__ bool wait_count_at_least(const uint32_t* p, uint32_t target) {
-    const long long t0 = clock64();
-    for (uint32_t it = 0; it < kFlagPollLimit; ++it) {
-        if (ld_acquire_gpu(p) >= target) return true;
-        if (waited_too_long(it, t0)) return false;
-        __nanosleep(32);
-    }
-    return false;
-}
-
-// Header of the pipelined step's synchronisation words: [0] = kPipeMagic and
-// [1] = the geometry key once the step's last kernel has reset the counters
-// after a step of the same geometry; anything else means "not armed", and
-// the kernels then wait for whole grids (programmatic dependent launch) as
-// the classic chain does.
-constexpr uint32_t kPipeMagic = 0x51535450u;   // 'QSTP'
-struct PipeSync {
-    uint32_t* header;    // [2]; null: classic chain
-    uint32_t* done;      // [batch]: score CTAs finished with request b
-    uint32_t* rowready;  // [batch * rows]: selection row ready
-    uint32_t key;        // geometry key of this step
-    int score_ctas;      // CTAs of the scoring grid (each counts once per request)
-};
-__device__ __forceinline__ bool pipe_armed(const PipeSync& s) {
-    return s.header != nullptr && ld_acquire_gpu(s.header) == kPipeMagic && ld_acquire_gpu(s.header + 1) == s.key;
-}
-
 // ---------------------------------------------------------------- tensor-core tiles
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                             uint32_t& r3) {

@@ -52,7 +52,6 @@ struct DecodeArgs {
     float scale_log2;         // softmax_scale * log2(e)
     float* o_part;            // [B][Hq][S][128] unnormalised partial outputs
     float2* ml_part;          // [B][Hq][S] (running max in log2 units, sum of exp2)
-    PipeSync ps;              // pipelined step: start a row when its selection is flagged
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -80,13 +79,6 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
 // channels, then it arrives on the stage's "empty" mbarrier.  The four warps'
 // running (max, sum, output) are merged through shared memory into the CTA's
 // partial.
-//
-// In the pipelined step (a.ps armed) a CTA does not wait for the whole top-K
-// grid: its producer polls the row's flag (release by the top-K CTA), then
-// lets the consumers go through a named barrier; the selection is read from
-// L2.  A CTA that is done leaves at once, so that the CTAs of the last
-// request find free slots while the top-K grid still waits for the scoring
-// grid; everything the combine reads is this grid's own output.
 __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(const __grid_constant__ DecodeArgs a,
                                                                           const __grid_constant__ CUtensorMap tmap_k,
                                                                           const __grid_constant__ CUtensorMap tmap_v) {
@@ -129,15 +121,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         prefetch_tmap(&tmap_v);
         const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
         const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
-        const bool armed = pipe_armed(a.ps);
-        if (armed) {
-            // sel_idx / sel_cnt of this row are flagged by its top-K CTA.
-            if (lane == 0 && a.sel_idx && !wait_count_at_least(a.ps.rowready + bg, 1u)) svq_flag(SV_DEVERR_TIMEOUT);
-            __syncwarp();
-            asm volatile("bar.arrive 2, %0;" ::"n"(kDecodeThreads) : "memory");
-        } else {
-            pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
-        }
+        pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
         int count = n;
         int spec_lp = -1;        // this lane's first list entry, fetched with the count
         bool spec_ok = false;    // true when the count is the one guessed below
@@ -148,8 +132,8 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
             const int chunk_g = (guess + a.num_splits - 1) / a.num_splits;
             const int j0_g = min(guess, split * chunk_g);
             const int my_g = min(guess, j0_g + chunk_g) - j0_g;
-            spec_lp = lane < my_g ? __ldcg(sel_row + j0_g + lane) : -1;
-            count = __ldcg(a.sel_cnt + bg);
+            spec_lp = lane < my_g ? sel_row[j0_g + lane] : -1;
+            count = a.sel_cnt[bg];
             spec_ok = count == guess;
             if (count < 0 || count > a.K || count > n) {
                 if (lane == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
@@ -172,7 +156,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
             phys_out = -1;
             valid_out = 0;
             if (ii < my_count) {
-                const int lp = sel_row ? (base == 0 && spec_ok ? spec_lp : __ldcg(sel_row + j0 + ii)) : j0 + ii;
+                const int lp = sel_row ? (base == 0 && spec_ok ? spec_lp : sel_row[j0 + ii]) : j0 + ii;
                 if (lp < 0 || lp >= n) {
                     svq_flag(SV_DEVERR_SEL_IDX);
                 } else {
@@ -242,12 +226,10 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
             qf[kk][1] = hv ? *reinterpret_cast<const uint32_t*>(qh + 16 * kk + 8 + 2 * quad) : 0u;
         }
     }
-    const bool armed = pipe_armed(a.ps);   // the same answer the producer got
-    if (armed) asm volatile("bar.sync 2, %0;" ::"n"(kDecodeThreads) : "memory");
-    else pdl_wait();
+    pdl_wait();
     // The producer's page count for this CTA (same formula, computed again here).
     int count = n;
-    if (a.sel_idx) count = max(0, min(__ldcg(a.sel_cnt + bg), min(a.K, n)));
+    if (a.sel_idx) count = max(0, min(a.sel_cnt[bg], min(a.K, n)));
     const int chunk = (count + a.num_splits - 1) / a.num_splits;
     const int j0 = min(count, split * chunk);
     const int my_count = min(count, j0 + chunk) - j0;
@@ -404,29 +386,14 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
 constexpr int kCombineThreads = 128;
 constexpr int kCombineBatch = 16;
 
-//
-// The last kernel of the pipelined step also resets that step's counters and
-// flags (every kernel that used them has completed by now) and then arms the
-// header, so that the next step of the same geometry on this workspace runs
-// pipelined.
 __global__ void __launch_bounds__(kCombineThreads) lse_combine_kernel(const float* __restrict__ o_part,
                                                                       const float2* __restrict__ ml_part,
                                                                       int num_splits, int64_t total_heads,
                                                                       __nv_bfloat16* __restrict__ out,
-                                                                      float* __restrict__ lse, const PipeSync ps,
-                                                                      int pipe_words) {
+                                                                      float* __restrict__ lse) {
     const int64_t qh = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     pdl_wait();   // partials come from the split kernel launched just before
-    if (ps.header != nullptr && blockIdx.x == 0 && threadIdx.x < 32) {
-        for (int i = lane; i < pipe_words; i += 32) ps.done[i] = 0u;   // done[] then rowready[], contiguous
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) {
-            ps.header[1] = ps.key;
-            st_release_gpu(ps.header, kPipeMagic);
-        }
-    }
     if (qh >= total_heads) return;
     const float2* ml = ml_part + qh * num_splits;
     const float* ob = o_part + qh * num_splits * kHeadDim + 4 * lane;
@@ -523,17 +490,12 @@ int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages,
 int launch_decode_fp8_split(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                             const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                             const int32_t* sel_cnt, int budget_pages, bool per_head, float softmax_scale, int splits,
-                            float* o_part, float2* ml_part, const PipeSync& ps, cudaStream_t stream);
+                            float* o_part, float2* ml_part, cudaStream_t stream);
 
-// ps (nullable): the pipelined step's synchronisation words, pipe_words of
-// them after ps->done (done[] and rowready[]).
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                   const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                   const int32_t* sel_cnt, int budget_pages, bool per_q_head, float softmax_scale, void* out,
-                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream,
-                  const PipeSync* ps, int pipe_words) {
-    const PipeSync none = {nullptr, nullptr, nullptr, 0u, 0};
-    const PipeSync& pipe = ps ? *ps : none;
+                  float* lse, void* workspace, size_t workspace_bytes, int sm_count, cudaStream_t stream) {
     static std::atomic<bool> attr_set[64];
     const int st0 = once_per_device(attr_set, [] {
         return cudaFuncSetAttribute(flash_decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -554,14 +516,13 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
         float2* ml_part8 = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) +
                                                      ((heads8 * kHeadDim * sizeof(float)) + 255) / 256 * 256);
         int st = launch_decode_fp8_split(c, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                                         budget_pages, per_head8, softmax_scale, splits8, o_part8, ml_part8, pipe,
-                                         stream);
+                                         budget_pages, per_head8, softmax_scale, splits8, o_part8, ml_part8, stream);
         if (st) return st;
         const int64_t total_heads8 = static_cast<int64_t>(batch) * num_q_heads;
         const int64_t blocks8 = (total_heads8 * 32 + kCombineThreads - 1) / kCombineThreads;
         return launch_pdl(lse_combine_kernel, dim3(static_cast<unsigned>(blocks8)), dim3(kCombineThreads), 0, stream,
                           static_cast<const float*>(o_part8), static_cast<const float2*>(ml_part8), splits8,
-                          total_heads8, static_cast<__nv_bfloat16*>(out), lse, pipe, pipe_words) == cudaSuccess
+                          total_heads8, static_cast<__nv_bfloat16*>(out), lse) == cudaSuccess
                    ? SV_OK
                    : SV_ERR_CUDA;
     }
@@ -604,7 +565,6 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     a.o_part = static_cast<float*>(workspace);
     a.ml_part = reinterpret_cast<float2*>(static_cast<unsigned char*>(workspace) +
                                           ((heads * kHeadDim * sizeof(float)) + 255) / 256 * 256);
-    a.ps = pipe;
     if (launch_pdl(flash_decode_split_kernel, dim3(splits, bh), dim3(kDecodeThreads), kDecodeSmem, stream, a, tmap_k,
                    tmap_v) != cudaSuccess)
         return SV_ERR_CUDA;
@@ -612,7 +572,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     const int64_t blocks = (total_heads * 32 + kCombineThreads - 1) / kCombineThreads;
     if (launch_pdl(lse_combine_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kCombineThreads), 0, stream,
                    static_cast<const float*>(a.o_part), static_cast<const float2*>(a.ml_part), splits, total_heads,
-                   static_cast<__nv_bfloat16*>(out), lse, pipe, pipe_words) != cudaSuccess)
+                   static_cast<__nv_bfloat16*>(out), lse) != cudaSuccess)
         return SV_ERR_CUDA;
     return SV_OK;
 }

@@ -66,7 +66,6 @@ struct DecodeF8Args {
     const float* v_scale;
     float* o_part;            // [B][Hq][S][128]
     float2* ml_part;          // [B][Hq][S]
-    PipeSync ps;              // pipelined step: start a row when its selection is flagged
 };
 
 __device__ __forceinline__ float f8_exp2(float x) {
@@ -127,15 +126,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         prefetch_tmap(&tmap_v);
         const int32_t* pt_row = a.page_table + static_cast<int64_t>(b) * a.max_pages;
         const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
-        const bool armed = pipe_armed(a.ps);
-        if (armed) {
-            // sel_idx / sel_cnt of this row are flagged by its top-K CTA.
-            if (lane == 0 && a.sel_idx && !wait_count_at_least(a.ps.rowready + bg, 1u)) svq_flag(SV_DEVERR_TIMEOUT);
-            __syncwarp();
-            asm volatile("bar.arrive 2, %0;" ::"n"(kF8Threads) : "memory");
-        } else {
-            pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
-        }
+        pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
         int count = n;
         int spec_lp = -1;        // this lane pair's first list entry, fetched with the count
         bool spec_ok = false;    // true when the count is the one guessed below
@@ -146,8 +137,8 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
             const int chunk_g = (guess + a.num_splits - 1) / a.num_splits;
             const int j0_g = min(guess, split * chunk_g);
             const int my_g = min(guess, j0_g + chunk_g) - j0_g;
-            spec_lp = (lane >> 1) < my_g ? __ldcg(sel_row + j0_g + (lane >> 1)) : -1;
-            count = __ldcg(a.sel_cnt + bg);
+            spec_lp = (lane >> 1) < my_g ? sel_row[j0_g + (lane >> 1)] : -1;
+            count = a.sel_cnt[bg];
             spec_ok = count == guess;
             if (count < 0 || count > a.K || count > n) {
                 if (lane == 0 && split == 0) svq_flag(SV_DEVERR_SEL_IDX);
@@ -166,7 +157,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
             phys_out = -1;
             valid_out = 0;
             if (i < my_count) {
-                const int lp = sel_row ? (i == u && spec_ok ? spec_lp : __ldcg(sel_row + j0 + i)) : j0 + i;
+                const int lp = sel_row ? (i == u && spec_ok ? spec_lp : sel_row[j0 + i]) : j0 + i;
                 if (lp < 0 || lp >= n) {
                     svq_flag(SV_DEVERR_SEL_IDX);
                 } else {
@@ -230,11 +221,9 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
             qf[mm][1] = pack_half2(bf16lo(w.y), bf16hi(w.y));
         }
     }
-    const bool armed = pipe_armed(a.ps);   // the same answer the producer got
-    if (armed) asm volatile("bar.sync 2, %0;" ::"n"(kF8Threads) : "memory");
-    else pdl_wait();
+    pdl_wait();
     int count = n;
-    if (a.sel_idx) count = max(0, min(__ldcg(a.sel_cnt + bg), min(a.K, n)));
+    if (a.sel_idx) count = max(0, min(a.sel_cnt[bg], min(a.K, n)));
     const int chunk = (count + a.num_splits - 1) / a.num_splits;
     const int j0 = min(count, split * chunk);
     const int my_count = min(count, j0 + chunk) - j0;
@@ -444,7 +433,7 @@ int decode_fp8_splits(const sv_cache* c, int batch, int rows_per_req, int pages,
 int launch_decode_fp8_split(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                             const int32_t* seq_lens, int batch, int max_pages, const int32_t* sel_idx,
                             const int32_t* sel_cnt, int budget_pages, bool per_head, float softmax_scale, int splits,
-                            float* o_part, float2* ml_part, const PipeSync& ps, cudaStream_t stream) {
+                            float* o_part, float2* ml_part, cudaStream_t stream) {
     const int64_t rows = c->num_phys_pages * c->num_kv_heads * kPage;
     if (rows > 0x7fffffffLL) return SV_ERR_UNSUPPORTED;
     CUtensorMap tmap_k, tmap_v;
@@ -470,7 +459,6 @@ int launch_decode_fp8_split(const sv_cache* c, const void* q, int num_q_heads, c
     a.v_scale = static_cast<const float*>(c->v_scale);
     a.o_part = o_part;
     a.ml_part = ml_part;
-    a.ps = ps;
     const int bh = batch * a.rows_per_req;
     return launch_pdl(flash_decode_fp8_kernel, dim3(splits, bh), dim3(kF8Threads), kF8Smem, stream, a, tmap_k,
                       tmap_v) == cudaSuccess

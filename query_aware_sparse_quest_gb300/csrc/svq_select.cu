@@ -409,317 +409,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     }
 }
 
-// ---------------------------------------------------------------- request-major scoring (pipelined step)
-//
-// The scoring kernel of the pipelined decode step: every CTA scores a slice
-// of every request, request after request (CTA x takes pages
-// [x n_b / X, (x + 1) n_b / X) of request b), so the batch's requests finish
-// one after another and the top-K of request b can start while later
-// requests are still being scored.  Each consumer lane keeps its
-// coefficients for the current request in registers and reloads them from
-// shared memory, where the whole batch's Qp / Qn are staged at the start
-// (batch x HKV <= kPipeMaxRows).  The producer streams the pages of all
-// slices back to back through the same ring, so no request boundary drains
-// it.  Consumers leave their scores in shared memory and count, per
-// request, the warps that are past it (CTA-scope release); a writer warp
-// copies a finished request's scores to global memory (coalesced), makes
-// them visible GPU-wide and adds one to done[b] (release), so only the
-// writer ever waits on a GPU-scope fence.  Request b is scored when done[b]
-// reaches X.  With done == nullptr (scores alone) the writer only copies.
-constexpr int kPipeMaxRows = 32;
-constexpr int kPipeWriter = kScoreConsumers + 1;            // warp index of the writer
-constexpr int kPipeThreads = (kScoreConsumers + 2) * 32;   // consumers, producer, writer
-
-// Its ring holds SVQ_PIPE_RING_KB of metadata (a multiple of the consumer
-// warps in slots).  The kernel streams at a rate set by its bytes in flight,
-// so the ring is as large as the length-split kernel's; a top-K CTA still
-// fits beside it on an SM, an attention CTA does not (attention starts as
-// scoring CTAs retire).
-#ifndef SVQ_PIPE_RING_KB
-#define SVQ_PIPE_RING_KB 128
-#endif
-template <int HKV>
-struct PipeShape {
-    static constexpr int kPageBytes = HKV * 2 * kHeadDim * 2;
-    static constexpr int kSlotsRaw = (SVQ_PIPE_RING_KB * 1024 / kPageBytes) / kScoreConsumers * kScoreConsumers;
-    static constexpr int kSlots = kSlotsRaw > 128 ? 128 : kSlotsRaw;
-    static constexpr int kRingBytes = kSlots * kPageBytes;
-    static constexpr int L = 32 / HKV;
-    static constexpr int C = HKV;
-    static_assert(kSlots % kScoreConsumers == 0 && kSlots >= kScoreConsumers, "ring slots");
-    static_assert(kSlots <= kScoreThreads, "one thread initialises each slot's barriers");
-};
-
-// Dynamic shared memory of the request-major scoring kernel: ring, the
-// batch's Qp / Qn, and the CTA's scores (each request's slice is at most
-// ceil(max_pages / X) pages).  The cap leaves room for a top-K CTA.
-constexpr int kPipeSmemCap = 184 * 1024;
-template <int HKV>
-int pipe_score_smem(int batch, int max_pages, int ctas) {
-    const int64_t per_req = (static_cast<int64_t>(max_pages) + ctas - 1) / ctas;
-    const int64_t bytes = PipeShape<HKV>::kRingBytes + static_cast<int64_t>(batch) * HKV * 2 * kHeadDim * 4 +
-                          static_cast<int64_t>(batch) * per_req * HKV * 4;
-    return bytes > (1 << 30) ? (1 << 30) : static_cast<int>(bytes);
-}
-
-template <int HKV>
-__global__ void __launch_bounds__(kPipeThreads, 1) score_pages_pipe_kernel(
-    const __nv_bfloat16* __restrict__ meta, int64_t num_phys_pages, const __nv_bfloat16* __restrict__ q,
-    int group, const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens, int max_pages,
-    float* __restrict__ scores, int batch, uint32_t* __restrict__ done) {
-    using S = PipeShape<HKV>;
-    constexpr int kSlots = S::kSlots, L = S::L, C = S::C;
-    constexpr int kConsumerThreads = kScoreConsumers * 32;
-    extern __shared__ __align__(128) unsigned char ring[];
-    float* const coef = reinterpret_cast<float*>(ring + S::kRingBytes);   // [batch][HKV][2][128]
-    float* const cta_scores = coef + batch * HKV * 2 * kHeadDim;          // [CTA's pages][HKV]
-    __shared__ __align__(8) uint64_t full_bar[kSlots];
-    __shared__ __align__(8) uint64_t empty_bar[kSlots];
-    __shared__ unsigned char slot_ok[kSlots];
-    __shared__ int s_lo[kPipeMaxRows], s_span[kPipeMaxRows], s_start[kPipeMaxRows + 1];
-    __shared__ unsigned int s_warps_done[kPipeMaxRows];
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int X = gridDim.x, x = blockIdx.x;
-    const uint32_t full0 = smem_addr(&full_bar[0]);
-    const uint32_t empty0 = smem_addr(&empty_bar[0]);
-
-    // This CTA's slice of every request, and where it starts in the CTA's
-    // sequence of pages (s_start: exclusive prefix over requests).
-    if (warp == 0) {
-        int n = 0;
-        if (lane < batch) {
-            const int len = seq_lens[lane];
-            n = (len + kPage - 1) / kPage;
-            if (len < 1 || n > max_pages) {
-                if (x == 0) svq_flag(SV_DEVERR_SEQ_LEN);
-                n = len < 1 ? 0 : max_pages;
-            }
-        }
-        const int lo = static_cast<int>(static_cast<int64_t>(x) * n / X);
-        const int hi = static_cast<int>(static_cast<int64_t>(x + 1) * n / X);
-        int incl = hi - lo;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        if (lane < batch) {
-            s_lo[lane] = lo;
-            s_span[lane] = hi - lo;
-            s_start[lane] = incl - (hi - lo);
-            s_warps_done[lane] = 0u;
-        }
-        if (lane == batch - 1) s_start[batch] = incl;
-    }
-    if (threadIdx.x < kSlots) {
-        mbar_init(full0 + threadIdx.x * 8, 1);
-        mbar_init(empty0 + threadIdx.x * 8, 1);
-        mbar_init_fence();
-    }
-    __syncthreads();
-    // The top-K kernel may be scheduled now: its CTAs wait on done[] for
-    // their request, not for this grid.
-    pdl_launch_dependents();
-    const int total = s_start[batch];
-
-    if (warp == kScoreProducer) {
-        // Lane l streams the CTA's pages l, l + 32, ...; (rb, rp) is the
-        // request and the offset in its slice of the lane's next page.
-        int rb = 0, rp = lane;
-        while (rb < batch && rp >= s_span[rb]) rp -= s_span[rb++];
-        auto entry = [&](int b, int p) { return page_table[static_cast<int64_t>(b) * max_pages + s_lo[b] + p]; };
-        int nxt = lane < total ? entry(rb, rp) : 0;
-        pdl_wait();   // metadata may come from an append launched just before
-        const unsigned char* meta_bytes = reinterpret_cast<const unsigned char*>(meta);
-        const uint32_t ring_s = smem_addr(ring);
-        int issued_last = -1;
-        bool failed = false;
-        for (int i = lane; i < total; i += 32) {
-            const int phys = nxt;
-            rp += 32;
-            while (rb < batch && rp >= s_span[rb]) rp -= s_span[rb++];
-            if (i + 32 < total) nxt = entry(rb, rp);
-            const int slot = i % kSlots;
-            if (i >= kSlots && !mbar_wait_bounded(empty0 + slot * 8, ((i / kSlots) - 1) & 1)) {
-                failed = true;
-                break;
-            }
-            const uint32_t fb = full0 + slot * 8;
-            const bool ok = static_cast<uint32_t>(phys) < static_cast<uint64_t>(num_phys_pages);
-            slot_ok[slot] = ok ? 1 : 0;
-            if (ok) {
-                mbar_arrive_expect_tx(fb, S::kPageBytes);
-                bulk_copy_g2s(ring_s + slot * S::kPageBytes, meta_bytes + static_cast<int64_t>(phys) * S::kPageBytes,
-                              S::kPageBytes, fb);
-            } else {
-                svq_flag(SV_DEVERR_PAGE_TABLE);
-                mbar_arrive(fb);
-            }
-            issued_last = i;
-        }
-        if (failed) svq_flag(SV_DEVERR_TIMEOUT);
-        // This lane's copies land before the CTA (and its shared memory)
-        // retires.  Only pages of the last kSlots are the final users of their
-        // slots (an earlier page's slot went on to a later page, whose phase
-        // the parity would then name): those are waited for; the copies of
-        // earlier pages landed before their slots were released.
-        for (int i = issued_last; i >= 0 && i >= total - kSlots; i -= 32)
-            (void)mbar_wait_bounded(full0 + (i % kSlots) * 8, (i / kSlots) & 1);
-        return;
-    }
-    if (warp == kPipeWriter) {
-        pdl_wait();   // the previous step's top-K may still read the score buffer
-        // Copies each request the consumers are done with, in order; one fence
-        // then covers every request copied since the last one, and those are
-        // published together (a fence lasts microseconds under load, so the
-        // writer never falls further behind than one fence).
-        auto consumers_done = [&](int r) {
-            uint32_t v;
-            asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr(&s_warps_done[r])) : "memory");
-            return v >= static_cast<uint32_t>(kScoreConsumers);
-        };
-        int copied = 0, published = 0;
-        const long long t0 = clock64();
-        uint32_t polls = 0;
-        bool gave_up = false;
-        while (published < batch) {
-            bool any = false;
-            while (copied < batch && (gave_up || __shfl_sync(0xffffffffu, consumers_done(copied), 0))) {
-                const int r = copied, span = s_span[r], base = s_start[r];
-                for (int j = 0; j < HKV; ++j) {
-                    float* dst = scores + (static_cast<int64_t>(r) * HKV + j) * max_pages + s_lo[r];
-                    for (int p = lane; p < span; p += 32) dst[p] = cta_scores[(base + p) * HKV + j];
-                }
-                ++copied;
-                any = true;
-            }
-            if (any) {
-                if (done != nullptr) {
-                    __threadfence();
-                    __syncwarp();
-                    if (lane == 0)
-                        for (int r = published; r < copied; ++r) red_release_gpu_add(done + r, 1u);
-                }
-                published = copied;
-            } else if (!gave_up) {
-                if (waited_too_long(polls++, t0)) {
-                    if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
-                    gave_up = true;   // copy and publish the rest as they are: no waiter is left waiting
-                } else {
-                    __nanosleep(32);
-                }
-            }
-        }
-        return;
-    }
-
-    // ---------------- consumer warps
-    // Fold every request's query heads into Qp / Qn: an item is 8 channels of
-    // one (request, kv head) (at most two items per thread); its group's rows
-    // of q are requested together (16-byte loads, one round trip per item),
-    // then summed head by head in order.
-    for (int item = threadIdx.x; item < batch * HKV * 16; item += kConsumerThreads) {
-        const int b = item / (HKV * 16), j = (item / 16) % HKV, c8 = item % 16;
-        uint4 rows[kMaxGroup];
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h)
-            rows[h] = h < group ? *reinterpret_cast<const uint4*>(
-                                      q + ((static_cast<int64_t>(b) * HKV + j) * group + h) * kHeadDim + c8 * 8)
-                                : make_uint4(0u, 0u, 0u, 0u);
-        float qp[8], qn[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) qp[e] = qn[e] = 0.f;
-#pragma unroll
-        for (int h = 0; h < kMaxGroup; ++h) {
-            if (h >= group) break;
-            const uint32_t v[4] = {rows[h].x, rows[h].y, rows[h].z, rows[h].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float lo = bf16lo(v[e]), hi = bf16hi(v[e]);
-                qp[2 * e] += fmaxf(lo, 0.f);
-                qn[2 * e] += fminf(lo, 0.f);
-                qp[2 * e + 1] += fmaxf(hi, 0.f);
-                qn[2 * e + 1] += fminf(hi, 0.f);
-            }
-        }
-        float* cb = coef + (b * HKV + j) * 2 * kHeadDim;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            cb[c8 * 8 + e] = qn[e];              // [0] pairs kmin
-            cb[kHeadDim + c8 * 8 + e] = qp[e];   // [1] pairs kmax
-        }
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory");
-
-    const int hj = lane / L;        // kv head of this lane
-    const int hk = lane % L;        // first chunk of this lane
-    // Requests [signaled, upto) are finished by this warp: count it in
-    // s_warps_done (release at CTA scope, after its scores in shared memory).
-    int signaled = 0;
-    auto signal_upto = [&](int upto) {
-        if (signaled >= upto) return;
-        __syncwarp();
-        if (lane == 0)
-            for (int r = signaled; r < upto; ++r)
-                asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(smem_addr(&s_warps_done[r])),
-                             "r"(1u)
-                             : "memory");
-        signaled = upto;
-    };
-    float c[C][8];
-    int cur_b = -1;
-    float* score_row = nullptr;   // this request's scores in shared memory, [page][HKV]
-    const unsigned char* lane_base = ring + hj * 512 + hk * 16;
-    int rb = 0, rp = warp;
-    while (rb < batch && rp >= s_span[rb]) rp -= s_span[rb++];
-    for (int i = warp; i < total; i += kScoreConsumers) {
-        if (rb != cur_b) {
-            signal_upto(rb);
-            cur_b = rb;
-            const float* cf = coef + (rb * HKV + hj) * 2 * kHeadDim;
-#pragma unroll
-            for (int t = 0; t < C; ++t) {
-                const int chunk = hk + L * t;   // chunks < 16 hold kmin channels, >= 16 kmax
-#pragma unroll
-                for (int e = 0; e < 8; ++e) c[t][e] = cf[(chunk >> 4) * kHeadDim + (chunk & 15) * 8 + e];
-            }
-            score_row = cta_scores + s_start[rb] * HKV + hj;
-        }
-        const int slot = i % kSlots;
-        const bool okw = mbar_wait_bounded(full0 + slot * 8, (i / kSlots) & 1);
-        if (__any_sync(0xffffffffu, !okw)) {
-            if (lane == 0) svq_flag(SV_DEVERR_TIMEOUT);
-            break;
-        }
-        uint4 w[C];
-#pragma unroll
-        for (int t = 0; t < C; ++t)
-            w[t] = *reinterpret_cast<const uint4*>(lane_base + slot * S::kPageBytes + t * L * 16);
-        const bool real = slot_ok[slot] != 0;
-        __syncwarp();   // every lane has read the slot before it is released
-        if (lane == 0) mbar_arrive(empty0 + slot * 8);
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int t = 0; t < C; ++t) {
-            const uint32_t xw[4] = {w[t].x, w[t].y, w[t].z, w[t].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                a0 = fmaf(c[t][2 * e], bf16lo(xw[e]), a0);
-                a1 = fmaf(c[t][2 * e + 1], bf16hi(xw[e]), a1);
-            }
-        }
-        float acc = real ? a0 + a1 : 0.f;
-#pragma unroll
-        for (int m = 1; m < L; m <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-        if (hk == 0) score_row[rp * HKV] = acc;
-        rp += kScoreConsumers;
-        while (rb < batch && rp >= s_span[rb]) rp -= s_span[rb++];
-    }
-    signal_upto(batch);   // also after a timeout, so that no waiter is left waiting
-}
-
 template <int HKV, bool PER_HEAD>
 int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const int32_t* page_table,
                      const int32_t* seq_lens, int batch, int max_pages, int sink, int window, float* scores,
@@ -759,38 +448,11 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
-template <int HKV>
-int launch_score_pipe_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const int32_t* page_table,
-                          const int32_t* seq_lens, int batch, int max_pages, float* scores, uint32_t* done,
-                          int ctas, cudaStream_t stream);
-int pipe_select_supported(int batch, int num_kv_heads, int max_pages, int sm_count);
-
-// Scores alone use the request-major kernel of the pipelined step (without
-// its counters) whenever the batch qualifies, so that one scoring kernel
-// serves both; SVQ_SCORE_REQUEST_MAJOR=0 keeps the length-split kernel.
-#ifndef SVQ_SCORE_REQUEST_MAJOR
-#define SVQ_SCORE_REQUEST_MAJOR 0
-#endif
-
 int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                  const int32_t* seq_lens, int batch, int max_pages, bool per_q_head, int sink, int window,
                  float* scores, int sm_count, cudaStream_t stream) {
     const int group = num_q_heads / c->num_kv_heads;
     const auto* qq = static_cast<const __nv_bfloat16*>(q);
-    if (SVQ_SCORE_REQUEST_MAJOR && !per_q_head && sink == 0 && window == 0 &&
-        pipe_select_supported(batch, c->num_kv_heads, max_pages, sm_count)) {
-        switch (c->num_kv_heads) {
-            case 1: return launch_score_pipe_hkv<1>(c, qq, group, page_table, seq_lens, batch, max_pages, scores,
-                                                    nullptr, sm_count, stream);
-            case 2: return launch_score_pipe_hkv<2>(c, qq, group, page_table, seq_lens, batch, max_pages, scores,
-                                                    nullptr, sm_count, stream);
-            case 4: return launch_score_pipe_hkv<4>(c, qq, group, page_table, seq_lens, batch, max_pages, scores,
-                                                    nullptr, sm_count, stream);
-            case 8: return launch_score_pipe_hkv<8>(c, qq, group, page_table, seq_lens, batch, max_pages, scores,
-                                                    nullptr, sm_count, stream);
-            default: return SV_ERR_UNSUPPORTED;
-        }
-    }
 #define SVQ_SCORE_CASE(H)                                                                                      \
     case H:                                                                                                    \
         return per_q_head ? launch_score_hkv<H, true>(c, qq, group, page_table, seq_lens, batch, max_pages,   \
@@ -825,10 +487,12 @@ int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_
 #ifndef SVQ_TOPK_THREADS
 #define SVQ_TOPK_THREADS 1024
 #endif
-constexpr int kTopkThreads = SVQ_TOPK_THREADS;   // the classic chain's CTA size
-constexpr int kTopkPipeThreads = 512;            // the pipelined step's: fits beside a scoring CTA
+constexpr int kTopkThreads = SVQ_TOPK_THREADS;
+constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kRadixBins = 2048;
+constexpr int kBinsPerThread = kRadixBins / kTopkThreads;
 constexpr int kCandCap = 256;
+static_assert(kRadixBins % kTopkThreads == 0 && kTopkWarps <= 32, "top-K block shape");
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t u = __float_as_uint(f);
@@ -841,7 +505,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 // before the block's next barrier, which saves a second one.
 template <bool reuse = true>
 __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* warp_tot) {
-    // (the block's warps, at most 32, each fold the totals of the warps before them)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -857,11 +520,8 @@ __device__ __forceinline__ uint32_t block_inclusive_scan(uint32_t v, uint32_t* w
 
 // Finds, over a 2048-bin histogram, the bin holding the `remaining`-th key
 // counted from the top, and how many keys of that bin are still needed.
-template <int THREADS>
 __device__ __forceinline__ void find_bin_from_top(const uint32_t* hist, uint32_t remaining, uint32_t* warp_tot,
                                                   uint32_t* s_bin, uint32_t* s_rem) {
-    constexpr int kBinsPerThread = kRadixBins / THREADS;
-    static_assert(kRadixBins % THREADS == 0 && THREADS / 32 <= 32, "top-K block shape");
     const int tid = threadIdx.x;
     // Thread t owns kBinsPerThread consecutive bins counted down from the top.
     const uint32_t top = kRadixBins - 1 - kBinsPerThread * tid;
@@ -886,26 +546,18 @@ __device__ __forceinline__ void find_bin_from_top(const uint32_t* hist, uint32_t
 }
 
 // Keys live in registers: thread t holds the ITEMS consecutive pages
-// [ITEMS t, ITEMS t + ITEMS) of the row (n <= ITEMS * THREADS), so the
+// [ITEMS t, ITEMS t + ITEMS) of the row (n <= ITEMS * kTopkThreads), so the
 // final compaction emits in ascending page order from per-thread bit masks.
-//
-// PIPE (the pipelined decode step): when the step's synchronisation words
-// are armed, the CTA waits for done[b] to count every scoring CTA instead of
-// for the whole scoring grid, reads the scores from L2 (they were written
-// during this kernel's lifetime), and after writing its row sets
-// rowready[row] (release) for the attention kernel.  Not armed: the classic
-// wait.  Either way the row flag is set.
-template <int ITEMS, int THREADS, bool PIPE>
-__global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __restrict__ scores,
-                                                             const int32_t* __restrict__ seq_lens,
-                                                             int num_kv_heads, int max_pages, int K,
-                                                             int32_t* __restrict__ sel_idx,
-                                                             int32_t* __restrict__ sel_cnt, const PipeSync ps) {
+template <int ITEMS>
+__global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* __restrict__ scores,
+                                                                  const int32_t* __restrict__ seq_lens,
+                                                                  int num_kv_heads, int max_pages, int K,
+                                                                  int32_t* __restrict__ sel_idx,
+                                                                  int32_t* __restrict__ sel_cnt) {
     static_assert(ITEMS <= 32, "selection masks are 32 bits");
-    constexpr int kWarps = THREADS / 32;
     __shared__ uint32_t hist[kRadixBins];
-    __shared__ uint32_t warp_tot[kWarps];
-    __shared__ uint32_t warp_lo[kWarps], warp_hi[kWarps];
+    __shared__ uint32_t warp_tot[kTopkWarps];
+    __shared__ uint32_t warp_lo[kTopkWarps], warp_hi[kTopkWarps];
     __shared__ uint32_t cand_key[kCandCap];
     __shared__ int32_t cand_idx[kCandCap];
     __shared__ uint32_t s_bin, s_rem, s_cand, s_T, s_take;
@@ -922,33 +574,16 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
     }
     const int m = min(K, n);
     int32_t* out = sel_idx + static_cast<int64_t>(bg) * K;
-    for (int i = tid; i < kRadixBins; i += THREADS) hist[i] = 0u;
+    for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
     if (tid == 0) s_cand = 0u;
     // The attention kernel that follows may start now: its CTAs set up and
-    // load q while this one runs, and wait (for the row flag, or for this
-    // grid's completion) before they read the selection.
+    // load q while this one runs, and wait for its completion before they
+    // read the selection.
     pdl_launch_dependents();
-    const bool armed = PIPE && pipe_armed(ps);
-    if (armed) {
-        if (tid == 0 && !wait_count_at_least(ps.done + b, static_cast<uint32_t>(ps.score_ctas)))
-            svq_flag(SV_DEVERR_TIMEOUT);
-        __syncthreads();
-    } else {
-        pdl_wait();   // scores come from the scoring kernel launched just before
-    }
-    // Publishes the row to the attention kernel (pipelined step).  The CTA
-    // then leaves at once, freeing its registers for attention CTAs.
-    auto publish = [&]() {
-        if constexpr (PIPE) {
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) st_release_gpu(ps.rowready + bg, 1u);
-        }
-    };
+    pdl_wait();   // scores come from the scoring kernel launched just before
     if (n <= K) {
-        for (int i = tid; i < K; i += THREADS) out[i] = i < n ? i : -1;
+        for (int i = tid; i < K; i += kTopkThreads) out[i] = i < n ? i : -1;
         if (tid == 0) sel_cnt[bg] = n;
-        publish();
         return;
     }
 
@@ -959,13 +594,12 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
     if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && i0 + ITEMS <= n) {
 #pragma unroll
         for (int e = 0; e < ITEMS; e += 4) {
-            const float4 v = PIPE ? __ldcg(reinterpret_cast<const float4*>(row + i0 + e))
-                                  : *reinterpret_cast<const float4*>(row + i0 + e);
+            const float4 v = *reinterpret_cast<const float4*>(row + i0 + e);
             f[e] = v.x; f[e + 1] = v.y; f[e + 2] = v.z; f[e + 3] = v.w;
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < ITEMS; ++e) f[e] = i0 + e < n ? (PIPE ? __ldcg(row + i0 + e) : row[i0 + e]) : 0.f;
+        for (int e = 0; e < ITEMS; ++e) f[e] = i0 + e < n ? row[i0 + e] : 0.f;
     }
     uint32_t key[ITEMS];
     uint32_t lo = 0xffffffffu, hi = 0u;
@@ -985,8 +619,8 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
     }
     __syncthreads();
     // Every warp folds the per-warp values itself (no second barrier).
-    lo = __reduce_min_sync(0xffffffffu, lane < kWarps ? warp_lo[lane] : 0xffffffffu);
-    hi = __reduce_max_sync(0xffffffffu, lane < kWarps ? warp_hi[lane] : 0u);
+    lo = __reduce_min_sync(0xffffffffu, lane < kTopkWarps ? warp_lo[lane] : 0xffffffffu);
+    hi = __reduce_max_sync(0xffffffffu, lane < kTopkWarps ? warp_hi[lane] : 0u);
     const uint32_t range = hi - lo;
     const int range_bits = range == 0 ? 0 : 32 - __clz(range);            // range < 2^bits
     const uint32_t shift = range_bits > 11 ? range_bits - 11 : 0;        // (range >> shift) < 2048
@@ -996,7 +630,7 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
     for (int e = 0; e < ITEMS; ++e)
         if (i0 + e < n) atomicAdd(&hist[(key[e] - lo) >> shift], 1u);
     __syncthreads();
-    find_bin_from_top<THREADS>(hist, static_cast<uint32_t>(m), warp_tot, &s_bin, &s_rem);
+    find_bin_from_top(hist, static_cast<uint32_t>(m), warp_tot, &s_bin, &s_rem);
     const uint32_t bstar = s_bin, need = s_rem;
     uint32_t T, take;
     if (hist[bstar] <= kCandCap) {
@@ -1057,13 +691,13 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
             const uint32_t nbins = 1u << kBits[pass];
             const uint32_t hi_mask = (pass == 0) ? 0u : ~((1u << (sh + kBits[pass])) - 1u);
             __syncthreads();
-            for (int i = tid; i < kRadixBins; i += THREADS) hist[i] = 0u;
+            for (int i = tid; i < kRadixBins; i += kTopkThreads) hist[i] = 0u;
             __syncthreads();
 #pragma unroll
             for (int e = 0; e < ITEMS; ++e)
                 if (i0 + e < n && (key[e] & hi_mask) == prefix) atomicAdd(&hist[(key[e] >> sh) & (nbins - 1u)], 1u);
             __syncthreads();
-            find_bin_from_top<THREADS>(hist, remaining, warp_tot, &s_bin, &s_rem);
+            find_bin_from_top(hist, remaining, warp_tot, &s_bin, &s_rem);
             prefix |= s_bin << sh;
             remaining = s_rem;
         }
@@ -1099,96 +733,25 @@ __global__ void __launch_bounds__(THREADS) topk_pages_kernel(const float* __rest
         if (pos < static_cast<uint32_t>(m)) out[pos] = i0 + e;
         ++pos;
     }
-    for (int i = m + tid; i < K; i += THREADS) out[i] = -1;
+    for (int i = m + tid; i < K; i += kTopkThreads) out[i] = -1;
     if (tid == 0) sel_cnt[bg] = m;
-    publish();
 }
 
 int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
                 int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, cudaStream_t stream) {
     cudaError_t e;
     const dim3 grid(batch * num_kv_heads), block(kTopkThreads);
-    const PipeSync none = {nullptr, nullptr, nullptr, 0u, 0};
     if (max_pages <= 8 * kTopkThreads)
-        e = launch_pdl(topk_pages_kernel<8, kTopkThreads, false>, grid, block, 0, stream, scores, seq_lens,
-                       num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, none);
+        e = launch_pdl(topk_pages_kernel<8>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
     else if (max_pages <= 16 * kTopkThreads)
-        e = launch_pdl(topk_pages_kernel<16, kTopkThreads, false>, grid, block, 0, stream, scores, seq_lens,
-                       num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, none);
+        e = launch_pdl(topk_pages_kernel<16>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
     else if (max_pages <= 32 * kTopkThreads)
-        e = launch_pdl(topk_pages_kernel<32, kTopkThreads, false>, grid, block, 0, stream, scores, seq_lens,
-                       num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, none);
+        e = launch_pdl(topk_pages_kernel<32>, grid, block, 0, stream, scores, seq_lens, num_kv_heads, max_pages,
+                       budget_pages, sel_idx, sel_cnt);
     else
         return SV_ERR_UNSUPPORTED;
-    return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-}
-
-// The pipelined step's selection: request-major scoring that counts finished
-// requests in ps.done, then top-K CTAs (kTopkPipeThreads) that start on a
-// request as soon as it is scored and flag their rows in ps.rowready.  Needs
-// batch * HKV <= kPipeMaxRows and max_pages <= 32 * kTopkPipeThreads.
-int pipe_select_supported(int batch, int num_kv_heads, int max_pages, int sm_count) {
-    if (batch * num_kv_heads > kPipeMaxRows || max_pages > 32 * kTopkPipeThreads) return 0;
-    switch (num_kv_heads) {
-        case 1: return pipe_score_smem<1>(batch, max_pages, sm_count) <= kPipeSmemCap;
-        case 2: return pipe_score_smem<2>(batch, max_pages, sm_count) <= kPipeSmemCap;
-        case 4: return pipe_score_smem<4>(batch, max_pages, sm_count) <= kPipeSmemCap;
-        case 8: return pipe_score_smem<8>(batch, max_pages, sm_count) <= kPipeSmemCap;
-        default: return 0;
-    }
-}
-
-template <int HKV>
-int launch_score_pipe_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const int32_t* page_table,
-                          const int32_t* seq_lens, int batch, int max_pages, float* scores, uint32_t* done,
-                          int ctas, cudaStream_t stream) {
-    using S = PipeShape<HKV>;
-    const int smem = pipe_score_smem<HKV>(batch, max_pages, ctas);
-    static std::atomic<bool> attr_set[64];
-    const int st = once_per_device(attr_set, [] {
-        return cudaFuncSetAttribute(score_pages_pipe_kernel<HKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kPipeSmemCap) == cudaSuccess
-                   ? SV_OK
-                   : SV_ERR_CUDA;
-    });
-    if (st) return st;
-    if (smem > kPipeSmemCap) return SV_ERR_UNSUPPORTED;
-    return launch_pdl(score_pages_pipe_kernel<HKV>, dim3(ctas), dim3(kPipeThreads), smem, stream,
-                      static_cast<const __nv_bfloat16*>(c->meta), c->num_phys_pages, q, group, page_table, seq_lens,
-                      max_pages, scores, batch, done) == cudaSuccess
-               ? SV_OK
-               : SV_ERR_CUDA;
-}
-
-int launch_select_pipe(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
-                       const int32_t* seq_lens, int batch, int max_pages, int budget_pages, float* scores,
-                       int32_t* sel_idx, int32_t* sel_cnt, const PipeSync& ps, cudaStream_t stream) {
-    const int group = num_q_heads / c->num_kv_heads;
-    const auto* qq = static_cast<const __nv_bfloat16*>(q);
-    int st;
-    switch (c->num_kv_heads) {
-        case 1: st = launch_score_pipe_hkv<1>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, ps.done,
-                                              ps.score_ctas, stream); break;
-        case 2: st = launch_score_pipe_hkv<2>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, ps.done,
-                                              ps.score_ctas, stream); break;
-        case 4: st = launch_score_pipe_hkv<4>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, ps.done,
-                                              ps.score_ctas, stream); break;
-        case 8: st = launch_score_pipe_hkv<8>(c, qq, group, page_table, seq_lens, batch, max_pages, scores, ps.done,
-                                              ps.score_ctas, stream); break;
-        default: return SV_ERR_UNSUPPORTED;
-    }
-    if (st) return st;
-    const dim3 grid(batch * c->num_kv_heads), block(kTopkPipeThreads);
-    cudaError_t e;
-    if (max_pages <= 8 * kTopkPipeThreads)
-        e = launch_pdl(topk_pages_kernel<8, kTopkPipeThreads, true>, grid, block, 0, stream, scores, seq_lens,
-                       c->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, ps);
-    else if (max_pages <= 16 * kTopkPipeThreads)
-        e = launch_pdl(topk_pages_kernel<16, kTopkPipeThreads, true>, grid, block, 0, stream, scores, seq_lens,
-                       c->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, ps);
-    else
-        e = launch_pdl(topk_pages_kernel<32, kTopkPipeThreads, true>, grid, block, 0, stream, scores, seq_lens,
-                       c->num_kv_heads, max_pages, budget_pages, sel_idx, sel_cnt, ps);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 

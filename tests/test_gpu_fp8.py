@@ -155,8 +155,7 @@ def test_fp8_decode_step_and_error_vs_bf16():
 def test_fp8_step_full_size_128k():
     """The benchmark's workload (8 requests of 128000 tokens, budget 256
     pages, shuffled 64000-page pool) on an fp8 pool through
-    sv_quest_decode_step, twice on one workspace (the first call whole kernel
-    after whole kernel, the second pipelined): every selection against the
+    sv_quest_decode_step, twice on one workspace: every selection against the
     oracle, attention of two sampled requests against the oracle's fp8
     decode over those selections, and the two calls bitwise equal."""
     wl, dw, host = _pair(synth.SPECS[2])

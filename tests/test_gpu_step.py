@@ -1,6 +1,5 @@
 """The one-call step (sv_quest_decode_step: page scores, top-K and sparse
-attention, pipelined by request when the batch allows) against the CPU oracle
-on the same seeded inputs.
+attention) against the CPU oracle on the same seeded inputs.
 
 Same bars as the separate calls: selected page sets exact except near-ties
 (fp32 scores within 1e-4 relative of the K-th score); bf16 outputs within
@@ -67,8 +66,8 @@ def test_step_parity(cfg):
 
 
 def test_step_repeatable_and_matches_separate_calls():
-    """Three calls give bitwise equal results, the last two on the workspace
-    the first left behind (the second and third run pipelined), and they
+    """Three calls give bitwise equal results, the last two on one workspace
+    that starts filled with garbage and is reused, and they
     agree with sv_quest_select + sv_sparse_decode: the same selection bit for
     bit (the same scores, the same exact top-K), attention within the bars."""
     pr = pair(2)
@@ -195,7 +194,7 @@ def test_step_budget_sweep_after_append():
         check_step(host, wl, gpu_step(dw, K, q=q), K, q=wl.step_q[0], seq_lens=seq)
 
 
-# ---------------------------------------------------------------- the pipelined one-call step
+# ---------------------------------------------------------------- a reused workspace
 
 def _flipped_q(wl):
     """The query with every sign flipped: other scores, another selection."""
@@ -204,14 +203,11 @@ def _flipped_q(wl):
 
 
 @pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
-def test_one_call_step_pipelined_after_the_first_call(cfg):
-    """The first sv_quest_decode_step on a workspace (garbage in it) waits for
-    whole grids and leaves the workspace's counters reset and armed; later
-    calls of the same geometry start each request's top-K and each row's
-    attention as soon as their inputs are done.  Every call matches the
-    oracle, also when q changes between calls, and equal inputs give bitwise
-    equal results on both paths.  (Batches of more than 32 request x kv head
-    rows always take the whole-grid chain.)"""
+def test_one_call_step_on_a_reused_workspace(cfg):
+    """Nothing in the workspace needs to start at zero or survives a call:
+    three calls on one workspace that starts filled with garbage, the second
+    with every sign of q flipped (other scores, another selection), each
+    match the oracle, and the first and third are bitwise equal."""
     pr = pair(cfg)
     wl, dw = pr.wl, pr.dw
     K = wl.spec.budget_pages
@@ -229,9 +225,9 @@ def test_one_call_step_pipelined_after_the_first_call(cfg):
 
 
 def test_one_call_step_workspace_shared_by_two_geometries():
-    """One workspace alternating between two batch geometries: each call finds
-    the other geometry's key in the header and takes the whole-grid chain,
-    and every result matches the oracle."""
+    """One workspace alternating between two batch geometries (each call
+    finds the other's scores and partials in it): every result matches the
+    oracle."""
     a = synth.SPECS[2].scaled(batch=4, ctx=16 * 500 + 3, needles_per_request=4, budget_pages=40)
     b = synth.SPECS[1].scaled(batch=6, ctx=16 * 300 + 9, budget_pages=24)
     pairs = []

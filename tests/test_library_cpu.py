@@ -145,12 +145,11 @@ def test_update_meta_rejects_bad_args(lib):
 
 def test_decode_step_workspace_size(lib):
     f = binding.sv_quest_decode_step_workspace_size
-    # select scores + sparse-decode partials + the pipelined step's words
-    # (a 2-word header, one count per request, one flag per (request, kv head))
+    # select scores + sparse-decode partials
     for args in ((8, 32, 4, 8000, 256), (2, 8, 1, 9000, 64), (32, 32, 4, 8192, 128)):
         B, Hq, Hkv, mp, K = args
         assert f(*args) >= (binding.sv_quest_select_workspace_size(B, Hkv, mp)
-                            + binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, K) + (2 + B + B * Hkv) * 4)
+                            + binding.sv_sparse_decode_workspace_size(B, Hq, Hkv, K))
     assert f(8, 32, 4, 8000, 256) < f(8, 32, 4, 8000, 512)
     assert f(0, 32, 4, 100, 16) == 0
     assert f(8, 32, 4, 100, 0) == 0
