@@ -320,6 +320,24 @@ def run_gpu(args):
 
     append_ms = float(np.mean(timed(append, max(3, min(args.steps, 200)))))
 
+    # A whole chunked prefill: request 0's tokens appended 4096 at a time (the
+    # pages' chunk_prefill_size), all chunks captured as one graph, so that
+    # back-to-back appends are timed as a prefill issues them.
+    L0 = int(wl.seq_lens[0])
+    k_all = resident.bf16_tensor(wl.k_tok[:L0], dev)
+    v_all = resident.bf16_tensor(wl.v_tok[:L0], dev)
+    slots_all = torch.from_numpy(wl.slot_mapping[:L0]).to(dev)
+    chunks = [(c0, min(L0, c0 + 4096)) for c0 in range(0, L0, 4096)]
+
+    def prefill():
+        for c0, c1 in chunks:
+            binding.sv_quest_update_meta(dw.cache, k_all[c0:c1], v_all[c0:c1], slots_all[c0:c1])
+
+    prefill()
+    g_prefill = capture(prefill)
+    prefill_ms = float(np.mean(timed(g_prefill.replay, max(3, min(args.steps // 10, 20)))))
+    del k_all, v_all, slots_all, g_prefill
+
     # ---- the same step over an fp8 (e4m3) pool of the same tokens
     dw8 = resident.upload(wl, device=dev, fp8=True)
     sel8, cnt8 = resident.select_buffers(B, Hkv, K, dev)
@@ -337,17 +355,68 @@ def run_gpu(args):
         lambda: binding.sv_sparse_decode(dw8.cache, dw8.q, dw8.page_table, dw8.seq_lens, sel8, cnt8, out8, lse8, ws),
         max(3, min(args.steps, 200)))))
     fp8_same_sel = bool(torch.equal(cnt8, sel_cnt))
-    del dw8
-    pages_touched = -(-T // spec.page_size)
-    append_bytes = (2 * T * Hkv * D * 2            # k_new, v_new read
-                    + 2 * T * Hkv * D * 2          # pool rows written
-                    + T * 4                        # slot mapping
-                    + pages_touched * Hkv * 2 * D * 2)   # metadata written
+    del dw8, g_step8
+
+    # ---- where selected K/V bytes dominate: 16 requests of 65536 tokens at a
+    # 512-page budget, the step over a bf16 and over an fp8 pool (each a CUDA
+    # graph, L2 flushed), and each sparse decode alone.
+    spec512 = synth.SPECS[4].scaled(budget_pages=512)
+    wl512 = synth.make_workload(spec512)
+    kv_heavy = {"workload": f"b{spec512.batch}_ctx{spec512.ctx}_budget{512 * spec512.page_size}"}
+    ab512 = algorithmic_bytes(wl512)
+    for fp8 in (False, True):
+        d5 = resident.upload(wl512, device=dev, fp8=fp8)
+        B5, Hq5, _ = d5.q.shape
+        Hkv5, K5, mp5 = spec512.num_kv_heads, 512, wl512.max_pages
+        s5, c5 = resident.select_buffers(B5, Hkv5, K5, dev)
+        o5 = torch.empty((B5, Hq5, D), dtype=torch.bfloat16, device=dev)
+        l5 = torch.empty((B5, Hq5), dtype=torch.float32, device=dev)
+        w5 = resident.workspace(binding.sv_quest_decode_step_workspace_size(B5, Hq5, Hkv5, mp5, K5), dev)
+        wd5 = resident.workspace(binding.sv_sparse_decode_workspace_size(B5, Hq5, Hkv5, K5), dev)
+
+        def step5():
+            binding.sv_quest_decode_step(d5.cache, d5.q, d5.page_table, d5.seq_lens, K5, s5, c5, o5, l5, w5)
+
+        def dec5():
+            binding.sv_sparse_decode(d5.cache, d5.q, d5.page_table, d5.seq_lens, s5, c5, o5, l5, wd5)
+
+        for _ in range(3):
+            step5()
+        g5 = capture(step5)
+        t5 = float(np.mean(timed(g5.replay, max(3, min(args.steps, 200)))))
+        td5 = float(np.mean(timed(dec5, max(3, min(args.steps, 200)))))
+        b_step = ab512["fp8_step" if fp8 else "step"]
+        b_dec = ab512["fp8_decode" if fp8 else "flash_decode_split_kernel"]
+        kv_heavy["fp8" if fp8 else "bf16"] = {
+            "ms_per_step": round(t5, 5), "bytes": b_step, "gbs": round(b_step / (t5 * 1e-3) / 1e9, 1),
+            "sparse_decode_ms": round(td5, 5), "decode_bytes": b_dec,
+            "decode_gbs": round(b_dec / (td5 * 1e-3) / 1e9, 1)}
+        del d5, g5, w5, wd5
+        torch.cuda.synchronize(dev)
+    kv_heavy["fp8_vs_bf16_step_time"] = round(kv_heavy["fp8"]["ms_per_step"] / kv_heavy["bf16"]["ms_per_step"], 4)
+    def append_bytes_of(T):
+        return (2 * T * Hkv * D * 2                      # k_new, v_new read
+                + 2 * T * Hkv * D * 2                    # pool rows written
+                + T * 4                                  # slot mapping
+                + -(-T // spec.page_size) * Hkv * 2 * D * 2)   # metadata written
+
+    append_bytes = append_bytes_of(T)
+    prefill_bytes = sum(append_bytes_of(c1 - c0) for c0, c1 in chunks)
 
     # ---- end to end through the public API: pinned host inputs in, results out
-    # The step's inputs (q, page table, lengths) sit in one pinned host block
-    # and its results (out, lse) in one device block, so each direction is a
-    # single copy; the device tensors the call receives are views of them.
+    # (a) The step's inputs (q, page table, lengths) and results (out, lse)
+    # live in page-locked host memory and are passed to sv_quest_decode_step
+    # as they are: its kernels read the inputs and write the results across
+    # the host link, so every step moves them host->device and device->host.
+    q_h, pt_h, sl_h = (t.cpu().pin_memory() for t in (dw.q, dw.page_table, dw.seq_lens))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step():
+        binding.sv_quest_decode_step(dw.cache, q_h, pt_h, sl_h, K, sel_idx, sel_cnt, out_h, lse_h, ws_step)
+
+    # (b) The same with copy-engine transfers: inputs in one pinned host block
+    # copied to one device block, results in one device block copied back.
     def packed(parts, device, pin):
         offs, total = [], 0
         for t in parts:
@@ -367,31 +436,28 @@ def run_gpu(args):
     res_d, (out_e, lse_e) = packed([out, lse], dev, False)
     res_h = torch.empty(res_d.numel(), dtype=torch.uint8).pin_memory()
 
-    def e2e_step():
+    def e2e_copy_step():
         in_d.copy_(in_h, non_blocking=True)
         binding.sv_quest_decode_step(dw.cache, q_d, pt_d, sl_d, K, sel_idx, sel_cnt, out_e, lse_e, ws_step)
         res_h.copy_(res_d, non_blocking=True)
 
-    # The whole end-to-end step (pinned host -> device copy, the public step
-    # call, device -> pinned host copy) is captured once as a CUDA graph, as a
-    # serving loop would, and replayed; the copies run inside every replay.
+    # Each end-to-end step is captured once as a CUDA graph, as a serving loop
+    # would, and replayed; the transfers run inside every replay.
     e2e_step()
+    e2e_copy_step()
     torch.cuda.synchronize(dev)
-    e2e_how = ("CUDA graph of: pinned host->device copy of q / page table / lengths (one block), "
-               "sv_quest_decode_step, device->pinned host copy of out / lse (one block)")
+    e2e_how = ("CUDA graph of sv_quest_decode_step with q / page table / lengths in page-locked host memory "
+               "and out / lse written into page-locked host memory by its kernels")
     e2e_eager_ms = float(np.mean(timed(e2e_step, max(3, min(args.steps, 200)))))
-    try:
-        g_e2e = capture(e2e_step)
-        e2e_run = g_e2e.replay
-    except RuntimeError as exc:      # copies from pinned memory not capturable here: time the eager calls
-        torch.cuda.synchronize(dev)
-        e2e_run = e2e_step
-        e2e_how = f"eager calls (graph capture refused: {str(exc)[:80]})"
-    e2e_ms = max_over_ranks(float(np.mean(timed(e2e_run, max(3, min(args.steps, 200))))), dev)
+    g_e2e = capture(e2e_step)
+    e2e_ms = max_over_ranks(float(np.mean(timed(g_e2e.replay, max(3, min(args.steps, 200))))), dev)
+    g_copy = capture(e2e_copy_step)
+    e2e_copy_ms = float(np.mean(timed(g_copy.replay, max(3, min(args.steps, 200)))))
     torch.cuda.synchronize(dev)
-    e2e_ok = bool(torch.equal(res_h[:out.numel() * 2].view(torch.bfloat16).view(out.shape).to(dev), out_e))
-    h2d = in_h.numel()
-    d2h = res_h.numel()
+    e2e_ok = bool(torch.equal(out_h.to(dev), out) and torch.equal(lse_h.to(dev), lse)
+                  and torch.equal(res_h[:out.numel() * 2].view(torch.bfloat16).view(out.shape).to(dev), out))
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, pt_h, sl_h))
+    d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h))
 
     torch.cuda.synchronize(dev)
     flags = binding.sv_get_device_error(reset=True)
@@ -439,7 +505,10 @@ def run_gpu(args):
         "e2e": {"value": round(whole_job_value(world, e2e_ms), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "how": e2e_how,
-                "eager_ms_per_step": round(e2e_eager_ms, 5), "result_copied_back": e2e_ok},
+                "eager_ms_per_step": round(e2e_eager_ms, 5), "result_copied_back": e2e_ok,
+                "copy_engine_ms_per_step": round(e2e_copy_ms, 5),
+                "copy_engine_how": "CUDA graph of: one pinned host->device copy of the inputs, "
+                                   "sv_quest_decode_step, one device->pinned host copy of the results"},
         "fp8_step": {"ms_per_step": round(fp8_ms, 5), "steps_per_s": round(1e3 / fp8_ms, 2),
                      "bytes": ab["fp8_step"], "gbs": round(ab["fp8_step"] / (fp8_ms * 1e-3) / 1e9, 1),
                      "sparse_decode_ms": round(fp8_dec_ms, 5),
@@ -447,7 +516,15 @@ def run_gpu(args):
                      "same_selection_counts": fp8_same_sel,
                      "note": "same step over an e4m3 K/V pool with per-row fp32 scales (bf16 metadata)"},
         "prefill_append": {"tokens": T, "ms": round(append_ms, 5), "bytes": append_bytes,
-                           "gbs": round(append_bytes / (append_ms * 1e-3) / 1e9, 1)},
+                           "gbs": round(append_bytes / (append_ms * 1e-3) / 1e9, 1),
+                           "note": "one 4096-token chunk, one eager call between events",
+                           "chunked_prefill": {
+                               "tokens": L0, "chunks": len(chunks), "ms": round(prefill_ms, 5),
+                               "ms_per_chunk": round(prefill_ms / len(chunks), 5), "bytes": prefill_bytes,
+                               "gbs": round(prefill_bytes / (prefill_ms * 1e-3) / 1e9, 1),
+                               "how": "request 0's tokens in 4096-token chunks, one sv_quest_update_meta per "
+                                      "chunk, all chunks one CUDA graph"}},
+        "kv_heavy_budget512": kv_heavy,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "gpu_launches_source": "kernels per call (sv_quest_decode_step: score 1 + top-K 1 + split decode 1 + combine 1), "

@@ -12,7 +12,12 @@
  *
  * Conventions common to every call
  *  - Every buffer argument is a DEVICE pointer, allocated and owned by the
- *    caller; the library never allocates, frees or retains it.
+ *    caller; the library never allocates, frees or retains it.  One
+ *    exception: the per-step inputs and results of sv_quest_decode_step (q,
+ *    page_table, seq_lens, out, lse) may be page-locked host memory that the
+ *    GPU addresses under unified addressing (e.g. from cudaHostAlloc).  Its
+ *    kernels then read those inputs and write those results across the
+ *    host link themselves, with no separate copy.
  *  - bf16 means IEEE bfloat16 stored as 16-bit words.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls enqueue kernels and return; they never synchronise.

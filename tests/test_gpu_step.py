@@ -241,3 +241,26 @@ def test_one_call_step_workspace_shared_by_two_geometries():
     for wl, dw, host in pairs + pairs + pairs[:1] + pairs[:1]:
         K = wl.spec.budget_pages
         check_step(host, wl, gpu_step(dw, K, ws=ws), K)
+
+
+def test_step_with_pinned_host_inputs_and_results():
+    """q, page table and lengths in page-locked host memory, out and lse
+    written straight into page-locked host memory: the kernels cross the host
+    link themselves.  The results equal the device-memory call bit for bit."""
+    pr = pair(1)
+    wl, dw = pr.wl, pr.dw
+    K = wl.spec.budget_pages
+    B, Hq, D = dw.q.shape
+    Hkv = dw.cache.num_kv_heads
+    ref = gpu_step(dw, K)
+    q_h, pt_h, sl_h = (t.cpu().pin_memory() for t in (dw.q, dw.page_table, dw.seq_lens))
+    out_h = torch.full((B, Hq, D), float("nan"), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.full((B, Hq), float("nan"), dtype=torch.float32).pin_memory()
+    sel_idx, sel_cnt = resident.select_buffers(B, Hkv, K)
+    ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, pt_h.shape[1], K))
+    binding.sv_quest_decode_step(dw.cache, q_h, pt_h, sl_h, K, sel_idx, sel_cnt, out_h, lse_h, ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(sel_idx.cpu().numpy(), ref[0]) and np.array_equal(sel_cnt.cpu().numpy(), ref[1])
+    assert np.array_equal(out_h.float().numpy(), ref[2], equal_nan=True)
+    assert np.array_equal(lse_h.numpy(), ref[3], equal_nan=True)
+    check_step(pr.host, wl, (sel_idx.cpu().numpy(), sel_cnt.cpu().numpy(), out_h.float().numpy(), lse_h.numpy()), K)
