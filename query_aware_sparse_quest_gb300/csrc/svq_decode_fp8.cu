@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const int32_t* sel_row = a.sel_idx ? a.sel_idx + static_cast<int64_t>(bg) * a.K : nullptr;
         pdl_wait();   // sel_idx / sel_cnt come from the top-K kernel launched just before
         int count = n;
-        int spec_lp = -1;        // this lane pair's first list entry, fetched with the count
+        int spec_lp = -1;        // this lane's first list entry, fetched with the count
         bool spec_ok = false;    // true when the count is the one guessed below
         if (a.sel_idx) {
             // The top-K writes min(K, n) entries; guess that count so that the
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
             const int chunk_g = (guess + a.num_splits - 1) / a.num_splits;
             const int j0_g = min(guess, split * chunk_g);
             const int my_g = min(guess, j0_g + chunk_g) - j0_g;
-            spec_lp = (lane >> 1) < my_g ? sel_row[j0_g + (lane >> 1)] : -1;
+            spec_lp = lane < my_g ? sel_row[j0_g + lane] : -1;
             count = a.sel_cnt[bg];
             spec_ok = count == guess;
             if (count < 0 || count > a.K || count > n) {
@@ -153,11 +153,14 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const uint32_t eb = empty0 + u * 8;
         const void* tmap = part ? static_cast<const void*>(&tmap_v) : static_cast<const void*>(&tmap_k);
         const float* scale_src = part ? a.v_scale : a.k_scale;
-        auto resolve = [&](int i, int& phys_out, int& valid_out) {
+        // Lane l resolves list position base + l to (physical page, valid
+        // tokens); the next 32 are resolved while the current 32 are issued.
+        auto resolve = [&](int base, int& phys_out, int& valid_out) {
+            const int i = base + lane;
             phys_out = -1;
             valid_out = 0;
             if (i < my_count) {
-                const int lp = sel_row ? (i == u && spec_ok ? spec_lp : sel_row[j0 + i]) : j0 + i;
+                const int lp = sel_row ? (base == 0 && spec_ok ? spec_lp : sel_row[j0 + i]) : j0 + i;
                 if (lp < 0 || lp >= n) {
                     svq_flag(SV_DEVERR_SEL_IDX);
                 } else {
@@ -171,29 +174,43 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
                 }
             }
         };
-        int phys, valid;
-        resolve(u, phys, valid);
+        int cur_phys, cur_valid, nxt_phys, nxt_valid;
+        resolve(0, cur_phys, cur_valid);
         int last = -1;
         bool ok = true;
-        for (int i = u; i < my_count; i += kF8Stages) {
-            int phys_next, valid_next;
-            resolve(i + kF8Stages, phys_next, valid_next);
-            if (i >= kF8Stages) ok = mbar_wait_bounded(eb, ((i / kF8Stages) - 1) & 1);
-            if (!ok) break;
-            if (part == 0) {
-                s_valid[u] = phys >= 0 ? valid : 0;
-                if (phys >= 0) mbar_arrive_expect_tx(fb, kF8Stage + kF8ScaleBytes);
-                else mbar_arrive(fb);
+        for (int base = 0; base < my_count && ok; base += 32) {
+            resolve(base + 32, nxt_phys, nxt_valid);
+            for (int sub = 0; sub < 32 && base + sub < my_count; sub += kF8Stages) {
+                // Lane pair u issues list position i = base + sub + u into stage u.
+                const int i = base + sub + u;
+                const int phys = __shfl_sync(0xffffffffu, cur_phys, sub + u);
+                const int valid = __shfl_sync(0xffffffffu, cur_valid, sub + u);
+                bool mine_ok = true;
+                if (i < my_count) {
+                    if (i >= kF8Stages) mine_ok = mbar_wait_bounded(eb, ((i / kF8Stages) - 1) & 1);
+                    if (mine_ok) {
+                        if (part == 0) {
+                            s_valid[u] = phys >= 0 ? valid : 0;
+                            if (phys >= 0) mbar_arrive_expect_tx(fb, kF8Stage + kF8ScaleBytes);
+                            else mbar_arrive(fb);
+                        }
+                        if (phys >= 0) {
+                            const int64_t head_row = static_cast<int64_t>(phys) * a.num_kv_heads + kvh;
+                            tma_load_2d(ring_s + u * kF8Stage + part * kF8Box, tmap, 0,
+                                        static_cast<int>(head_row * kPage), fb);
+                            bulk_copy_g2s(scale_s + u * kF8ScaleBytes + part * (kPage * 4),
+                                          scale_src + head_row * kPage, kPage * 4, fb);
+                        }
+                        last = i;
+                    }
+                }
+                if (__any_sync(0xffffffffu, !mine_ok)) {
+                    ok = false;
+                    break;
+                }
             }
-            if (phys >= 0) {
-                const int64_t head_row = static_cast<int64_t>(phys) * a.num_kv_heads + kvh;
-                tma_load_2d(ring_s + u * kF8Stage + part * kF8Box, tmap, 0, static_cast<int>(head_row * kPage), fb);
-                bulk_copy_g2s(scale_s + u * kF8ScaleBytes + part * (kPage * 4), scale_src + head_row * kPage,
-                              kPage * 4, fb);
-            }
-            last = i;
-            phys = phys_next;
-            valid = valid_next;
+            cur_phys = nxt_phys;
+            cur_valid = nxt_valid;
         }
         if (!ok) svq_flag(SV_DEVERR_TIMEOUT);
         // This lane's copies land before the CTA (and its shared memory) retires.
