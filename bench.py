@@ -552,6 +552,73 @@ def step_bytes(wl, budget_pages, appended=0):
     return b
 
 
+def run_only(args):
+    """One call type alone on the benchmark workload, for profiling with a
+    small device footprint (one bf16 or fp8 pool): --only step (the one-call
+    decode step, as a CUDA graph), append (one 4096-token sv_quest_update_meta)
+    or fp8_step (the step over an fp8 pool).  W untimed and K timed calls, each
+    after an L2 flush; prints one JSON line with the mean time per call."""
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    build.build()
+    spec = synth.SPECS[BENCH_CONFIG]
+    wl = synth.make_workload(spec)
+    dw = resident.upload(wl, device=dev, fp8=args.only == "fp8_step")
+    B, Hq, D = dw.q.shape
+    Hkv, K = spec.num_kv_heads, spec.budget_pages
+    sel_idx, sel_cnt = resident.select_buffers(B, Hkv, K, dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, Hkv, wl.max_pages, K), dev)
+    if args.only == "append":
+        T = min(4096, int(wl.seq_lens[0]))
+        k_new = resident.bf16_tensor(wl.k_tok[:T], dev)
+        v_new = resident.bf16_tensor(wl.v_tok[:T], dev)
+        slots = torch.from_numpy(wl.slot_mapping[:T]).to(dev)
+
+        def call():
+            binding.sv_quest_update_meta(dw.cache, k_new, v_new, slots)
+    else:
+        def step():
+            binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse,
+                                         ws)
+
+        step()
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        call = graph.replay
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
+    for _ in range(args.warmup):
+        flush_w.zero_()
+        flush_r.sum()
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize(dev)
+    for e0, e1 in evs:
+        flush_w.zero_()
+        flush_r.sum()
+        e0.record()
+        call()
+        e1.record()
+    torch.cuda.synchronize(dev)
+    ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in evs]))
+    flags = binding.sv_get_device_error(reset=True)
+    if flags:
+        raise SystemExit(f"device error word {flags:#x}")
+    print(json.dumps({"only": args.only, "workload": spec.name, "calls": args.steps, "warmup": args.warmup,
+                      "ms_per_call": round(ms, 5)}), flush=True)
+
+
 def run_all_configs(args):
     """One JSON line per workload: the step (sv_quest_decode_step, CUDA graph,
     L2 flushed before each replay, median of the timed replays) and the dense
@@ -746,8 +813,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--all-configs", action="store_true",
                     help="instead of the benchmark line, one line per workload (step and dense timings)")
+    ap.add_argument("--only", choices=["step", "append", "fp8_step"],
+                    help="time one call type alone on the benchmark workload (for profiling), no benchmark line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
+    if args.only:
+        run_only(args)
+        return
     if args.all_configs:
         run_all_configs(args)
         return
