@@ -447,7 +447,8 @@ def run_gpu(args):
     e2e_copy_step()
     torch.cuda.synchronize(dev)
     e2e_how = ("CUDA graph of sv_quest_decode_step with q / page table / lengths in page-locked host memory "
-               "and out / lse written into page-locked host memory by its kernels")
+               "(q staged into the workspace by one copy kernel) and out / lse written into page-locked host "
+               "memory by its kernels")
     e2e_eager_ms = float(np.mean(timed(e2e_step, max(3, min(args.steps, 200)))))
     g_e2e = capture(e2e_step)
     e2e_ms = max_over_ranks(float(np.mean(timed(g_e2e.replay, max(3, min(args.steps, 200))))), dev)

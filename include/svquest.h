@@ -285,6 +285,10 @@ int sv_sparse_decode_static_scratch(const sv_cache* cache, const void* q, int32_
  *  - workspace: sv_quest_decode_step_workspace_size(...) bytes, not shared
  *    with a call that may run at the same time; nothing in it needs to start
  *    at zero.
+ *  - A q in page-locked host memory is first copied into the workspace by
+ *    one small kernel (each of its bytes crosses the host link once; every
+ *    scoring CTA of a request reads that request's query), and the
+ *    kernels then read the copy.
  */
 int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_heads,
                          const int32_t* page_table, const int32_t* seq_lens, int32_t batch,

@@ -1,6 +1,8 @@
 // C ABI of libsvquest.so (include/svquest.h): host-side argument checks,
-// launch-shape choices and dispatch to the kernels.  Nothing here allocates,
-// frees or synchronises, except sv_get_device_error which reads device words.
+// launch-shape choices and dispatch to the kernels, plus the small kernel that
+// stages a host-resident query for the one-call step.  Nothing here
+// allocates, frees or synchronises, except sv_get_device_error which reads
+// device words.
 #include <climits>
 
 #include "svq_common.cuh"
@@ -13,7 +15,7 @@ int launch_update_meta(const sv_cache* c, const void* k_new, const void* v_new, 
                        int64_t num_tokens, cudaStream_t stream);
 int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                  const int32_t* seq_lens, int batch, int max_pages, bool per_q_head, int sink, int window,
-                 float* scores, int sm_count, cudaStream_t stream);
+                 float* scores, int sm_count, cudaStream_t stream, int q_after_wait);
 int launch_topk(const float* scores, const int32_t* seq_lens, int batch, int num_kv_heads, int max_pages,
                 int budget_pages, int32_t* sel_idx, int32_t* sel_cnt, cudaStream_t stream);
 int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
@@ -79,6 +81,35 @@ int check_batch(const void* q, const int32_t* page_table, const int32_t* seq_len
 size_t scores_bytes(int batch, int rows_per_req, int max_pages) {
     return (static_cast<size_t>(batch) * rows_per_req * max_pages * sizeof(float) + 255) / 256 * 256;
 }
+size_t query_bytes(int batch, int num_q_heads) {
+    return (static_cast<size_t>(batch) * num_q_heads * 128 * 2 + 255) / 256 * 256;
+}
+
+// True when p is page-locked host memory.  Device, managed and unregistered
+// memory answer false; a failed query also answers false and its error is
+// cleared, so that it does not surface in the caller's next error check.
+bool is_pinned_host(const void* p) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    return a.type == cudaMemoryTypeHost;
+}
+
+// Copies a query that lives in page-locked host memory into the workspace,
+// so that each of its bytes crosses the host link once (the scoring kernel
+// reads a request's query from each of that request's CTAs).  The loads come
+// before the wait on the kernel before, which may still read the previous
+// copy; the stores come after it.
+__global__ void __launch_bounds__(256) stage_query_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                          int64_t n16) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const uint4 v = i < n16 ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+    svq::pdl_wait();
+    svq::pdl_launch_dependents();
+    if (i < n16) dst[i] = v;
+}
 
 const sv_quest_opts kBaseOpts = {0, 0, 0, 0, 0};
 
@@ -114,7 +145,7 @@ int select_impl(const sv_cache* cache, const void* q, int32_t num_q_heads, const
     if ((st = sm_count_of_current_device(&sms))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, opts->per_q_head != 0,
-                           opts->sink_pages, opts->window_pages, scores, sms, s)))
+                           opts->sink_pages, opts->window_pages, scores, sms, s, 0)))
         return st;
     return launch_topk(scores, seq_lens, batch, rows, max_pages, budget_pages, sel_idx, sel_cnt, s);
 }
@@ -171,7 +202,7 @@ int sv_quest_score(const sv_cache* cache, const void* q, int32_t num_q_heads, co
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     return launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms,
-                        static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream), 0);
 }
 
 int sv_quest_topk(const float* scores, const int32_t* seq_lens, int32_t batch, int32_t num_kv_heads,
@@ -237,8 +268,8 @@ int sv_sparse_decode_ex(const sv_cache* cache, const void* q, int32_t num_q_head
 size_t sv_quest_decode_step_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t max_pages, int32_t budget_pages) {
     if (batch < 1 || num_q_heads < 1 || num_kv_heads < 1 || max_pages < 1 || budget_pages < 1) return 0;
-    // Scores at the front, split-K partials after.
-    return scores_bytes(batch, num_kv_heads, max_pages) +
+    // Scores, room for a copy of a host-resident query, split-K partials.
+    return scores_bytes(batch, num_kv_heads, max_pages) + query_bytes(batch, num_q_heads) +
            decode_workspace_bytes(batch, num_q_heads, decode_max_splits(budget_pages));
 }
 
@@ -277,17 +308,29 @@ int sv_quest_decode_step(const sv_cache* cache, const void* q, int32_t num_q_hea
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // Scores at the front of the workspace, split-K partials after.
+    // Workspace: scores, a copy of the query when it lives in page-locked
+    // host memory, then the split-K partials.
     const int hkv = cache->num_kv_heads;
     const size_t sb = scores_bytes(batch, hkv, max_pages);
-    float* scores = static_cast<float*>(workspace);
-    if ((st = launch_score(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s)))
+    const size_t qb = query_bytes(batch, num_q_heads);
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    float* scores = reinterpret_cast<float*>(ws);
+    const void* qd = q;
+    const bool staged = is_pinned_host(q);
+    if (staged) {
+        const int64_t n16 = static_cast<int64_t>(batch) * num_q_heads * 128 * 2 / 16;
+        if (launch_pdl(stage_query_kernel, dim3(static_cast<unsigned>((n16 + 255) / 256)), dim3(256), 0, s,
+                       static_cast<const uint4*>(q), reinterpret_cast<uint4*>(ws + sb), n16) != cudaSuccess)
+            return SV_ERR_CUDA;
+        qd = ws + sb;
+    }
+    if ((st = launch_score(cache, qd, num_q_heads, page_table, seq_lens, batch, max_pages, false, 0, 0, scores, sms, s,
+                           staged ? 1 : 0)))
         return st;
     if ((st = launch_topk(scores, seq_lens, batch, hkv, max_pages, budget_pages, sel_idx, sel_cnt, s)))
         return st;
-    return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
-                         budget_pages, false, softmax_scale, out, lse, static_cast<unsigned char*>(workspace) + sb,
-                         workspace_bytes - sb, sms, s);
+    return launch_decode(cache, qd, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
+                         budget_pages, false, softmax_scale, out, lse, ws + sb + qb, workspace_bytes - sb - qb, sms, s);
 }
 
 int sv_get_device_error(uint32_t* flags, int reset) {

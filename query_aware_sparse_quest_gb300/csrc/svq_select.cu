@@ -144,7 +144,7 @@ template <int HKV, bool PER_HEAD>
 __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     const __nv_bfloat16* __restrict__ meta, int64_t num_phys_pages, const __nv_bfloat16* __restrict__ q,
     int group, const int32_t* __restrict__ page_table, const int32_t* __restrict__ seq_lens, int max_pages,
-    int pages_per_cta, int sink, int window, float* __restrict__ scores, int batch) {
+    int pages_per_cta, int sink, int window, float* __restrict__ scores, int batch, int q_after_wait) {
     using S = ScoreShape<HKV>;
     constexpr int kSlots = S::kSlots, L = S::L, C = S::C;
     extern __shared__ __align__(128) unsigned char ring[];
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
     constexpr int kQVecs = (HKV * kMaxGroup * kHeadDim / 8 + kConsumerThreads - 1) / kConsumerThreads;
     const int hq = HKV * group;
     uint4 qpre[kQVecs];
-    if (warp != kScoreProducer) {
+    if (warp != kScoreProducer && !q_after_wait) {
         const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
 #pragma unroll
         for (int i = 0; i < kQVecs; ++i) {
@@ -248,10 +248,13 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         // kv group's query heads into Qp / Qn, while the producer already
         // streams metadata.  q is an input of the step, so this also overlaps
         // the previous kernel.
+        // With q_after_wait the query is written by the kernel launched just
+        // before (a copy of a host-resident query): wait for it first.
+        if (q_after_wait) pdl_wait();
         {
             const uint4* qsrc = reinterpret_cast<const uint4*>(q + static_cast<int64_t>(b) * hq * kHeadDim);
             uint4* qdst = reinterpret_cast<uint4*>(qstage);
-            const bool kept = b == guess_b;
+            const bool kept = b == guess_b && !q_after_wait;
 #pragma unroll
             for (int i = 0; i < kQVecs; ++i) {
                 const int v = threadIdx.x + i * kConsumerThreads;
@@ -412,7 +415,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
 template <int HKV, bool PER_HEAD>
 int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const int32_t* page_table,
                      const int32_t* seq_lens, int batch, int max_pages, int sink, int window, float* scores,
-                     int sm_count, cudaStream_t stream) {
+                     int sm_count, cudaStream_t stream, int q_after_wait) {
     using S = ScoreShape<HKV>;
     static std::atomic<bool> attr_set[64];
     const int st = once_per_device(attr_set, [] {
@@ -444,21 +447,21 @@ int launch_score_hkv(const sv_cache* c, const __nv_bfloat16* q, int group, const
     const cudaError_t e = launch_pdl(score_pages_kernel<HKV, PER_HEAD>, grid, dim3(kScoreThreads), S::kSmemBytes,
                                      stream, static_cast<const __nv_bfloat16*>(c->meta), c->num_phys_pages, q, group,
                                      page_table, seq_lens, max_pages, static_cast<int>(ppc), sink, window, scores,
-                                     batch);
+                                     batch, q_after_wait);
     return e == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_t* page_table,
                  const int32_t* seq_lens, int batch, int max_pages, bool per_q_head, int sink, int window,
-                 float* scores, int sm_count, cudaStream_t stream) {
+                 float* scores, int sm_count, cudaStream_t stream, int q_after_wait) {
     const int group = num_q_heads / c->num_kv_heads;
     const auto* qq = static_cast<const __nv_bfloat16*>(q);
 #define SVQ_SCORE_CASE(H)                                                                                      \
     case H:                                                                                                    \
         return per_q_head ? launch_score_hkv<H, true>(c, qq, group, page_table, seq_lens, batch, max_pages,   \
-                                                      sink, window, scores, sm_count, stream)                 \
+                                                      sink, window, scores, sm_count, stream, q_after_wait)   \
                           : launch_score_hkv<H, false>(c, qq, group, page_table, seq_lens, batch, max_pages,  \
-                                                       sink, window, scores, sm_count, stream);
+                                                       sink, window, scores, sm_count, stream, q_after_wait);
     switch (c->num_kv_heads) {
         SVQ_SCORE_CASE(1)
         SVQ_SCORE_CASE(2)

@@ -264,3 +264,23 @@ def test_step_with_pinned_host_inputs_and_results():
     assert np.array_equal(out_h.float().numpy(), ref[2], equal_nan=True)
     assert np.array_equal(lse_h.numpy(), ref[3], equal_nan=True)
     check_step(pr.host, wl, (sel_idx.cpu().numpy(), sel_cnt.cpu().numpy(), out_h.float().numpy(), lse_h.numpy()), K)
+    # The same call captured in a CUDA graph (as a serving loop would) and replayed.
+    out_h.fill_(float("nan"))
+    lse_h.fill_(float("nan"))
+
+    def call():
+        binding.sv_quest_decode_step(dw.cache, q_h, pt_h, sl_h, K, sel_idx, sel_cnt, out_h, lse_h, ws)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    out_h.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(out_h.float().numpy(), ref[2], equal_nan=True)
+    assert np.array_equal(lse_h.numpy(), ref[3], equal_nan=True)
