@@ -50,7 +50,7 @@ template <bool FP8>
 __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __restrict__ scale,
                                            __nv_bfloat16* __restrict__ meta, bool is_key, int num_kv_heads, int h,
                                            const __nv_bfloat16* __restrict__ rows_new, int64_t t, int R, int32_t si,
-                                           int first) {
+                                           int first, const uint4* staged) {
     const int lane = threadIdx.x & 31;
     const int32_t slot = __shfl_sync(0xffffffffu, si, first);
     const int64_t page = slot / kPage;
@@ -61,7 +61,9 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
     for (int k = 0; k < kPage / 2; ++k) {
         const int r = half + 2 * k;
         kw[k] = make_uint4(0u, 0u, 0u, 0u);
-        if (r < R) kw[k] = *reinterpret_cast<const uint4*>(rows_new + ((t + r) * num_kv_heads + h) * kHeadDim + c * 8);
+        if (r < R)
+            kw[k] = staged ? staged[32 * k]
+                           : *reinterpret_cast<const uint4*>(rows_new + ((t + r) * num_kv_heads + h) * kHeadDim + c * 8);
     }
 #pragma unroll
     for (int k = 0; k < kPage / 2; ++k) {
@@ -161,23 +163,46 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_meta_kernel(
     const int32_t* __restrict__ slot_mapping, int64_t num_tokens, int win) {
     const int lane = threadIdx.x & 31;
     const int64_t item = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    // The kernel before may still read the pool and the metadata: wait for
-    // it before writing.  The scoring kernel that usually follows may then
-    // be scheduled and load its page-table entries and query meanwhile.
-    pdl_wait();
-    pdl_launch_dependents();
     const int64_t windows = (num_tokens + win - 1) / win;
-    if (item >= windows * num_kv_heads * 2) return;
+    const bool active = item < windows * num_kv_heads * 2;
     const bool is_key = (item & 1) == 0;                        // even items: keys, odd: values
     const int64_t t0 = (item / 2 / num_kv_heads) * win;
     const int h = static_cast<int>((item / 2) % num_kv_heads);
     const int64_t pool_slots = num_phys_pages * kPage;
     auto in_pool = [&](int32_t sl) { return sl >= 0 && sl < pool_slots; };
+    const __nv_bfloat16* rows_new = is_key ? k_new : v_new;
 
+    // The slots and new rows are inputs of the call, so they load before the
+    // wait for the kernel before (which may still read or write the pool and
+    // the metadata): in a chunked prefill a chunk's loads then overlap the
+    // previous chunk's stores.  The rows of a run starting at the window's
+    // first token (a prefill window's only run) go to shared memory by async
+    // copies (lane l: chunk l % 16 of rows l / 16 + 2 k), which hold no
+    // registers; other runs load theirs when they are handled.
+    __shared__ __align__(16) uint4 s_rows[kAppendThreads / 32][kPage / 2][32];
+    uint4* const my_rows = &s_rows[threadIdx.x >> 5][0][lane];
+    {
+        const int c = lane & 15, half = lane >> 4;
+#pragma unroll
+        for (int k = 0; k < kPage / 2; ++k) {
+            const int64_t t = t0 + half + 2 * k;
+            const bool ok = active && t < num_tokens;
+            cp_async16(smem_addr(my_rows + 32 * k), ok ? rows_new + (t * num_kv_heads + h) * kHeadDim + c * 8 : rows_new,
+                       ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    }
     // 1. slots of tokens t0 .. t0 + 31 and of t0 - 1; runs that start in the window.
     const int64_t ti = t0 + lane;
-    const int32_t si = ti < num_tokens ? slot_mapping[ti] : -1;
-    const int32_t s_before = (lane == 0 && t0 > 0) ? slot_mapping[t0 - 1] : -1;
+    const int32_t si = active && ti < num_tokens ? slot_mapping[ti] : -1;
+    const int32_t s_before = (active && lane == 0 && t0 > 0) ? slot_mapping[t0 - 1] : -1;
+    cp_async_wait<0>();   // each lane reads back only its own copies
+    // The kernel before may still read the pool and the metadata: wait for
+    // it before writing.  The scoring kernel that usually follows may then
+    // be scheduled and load its page-table entries and query meanwhile.
+    pdl_wait();
+    pdl_launch_dependents();
+    if (!active) return;
     if (lane < win && ti < num_tokens && !in_pool(si) && h == 0 && is_key) svq_flag(SV_DEVERR_SLOT);
     int32_t sp = __shfl_up_sync(0xffffffffu, si, 1);   // the predecessor's slot
     if (lane == 0) sp = s_before;
@@ -190,7 +215,7 @@ __global__ void __launch_bounds__(kAppendThreads) append_kv_meta_kernel(
         starts &= starts - 1u;
         const int R = __ffs(~(cont_mask >> (r + 1)));   // 1 + the continuing tokens after r (r + R <= 31)
         append_run<FP8>(is_key ? k_pool : v_pool, is_key ? k_scale : v_scale, meta, is_key, num_kv_heads, h,
-                        is_key ? k_new : v_new, t0 + r, R, si, r);
+                        rows_new, t0 + r, R, si, r, r == 0 ? my_rows : nullptr);
     }
 }
 
