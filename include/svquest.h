@@ -22,9 +22,10 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls enqueue kernels and return; they never synchronise.
  *  - Kernels are launched with programmatic dependent launch.  The scoring,
- *    top-K and attention kernels read the call's q, page_table and seq_lens
- *    as soon as they start, possibly while the kernel enqueued just before
- *    them is still running.  Pools, metadata and workspace are touched only
+ *    top-K and attention kernels read the call's q, page_table and seq_lens,
+ *    and the append kernel its slot_mapping, k_new and v_new, as soon as
+ *    they start, possibly while the kernel enqueued just before them is
+ *    still running.  Pools, metadata and workspace are touched only
  *    after that kernel has completed.  So the kernel that produces a
  *    call's inputs must not release its dependents early
  *    (griddepcontrol.launch_dependents): an ordinary kernel, a copy, or any
