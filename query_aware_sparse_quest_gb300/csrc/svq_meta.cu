@@ -26,6 +26,14 @@ SVQ_DEFINE_ERROR_WORD(read_error_meta)
 // 16-token window) take win = 16, so every warp of the grid has a run; short
 // ones (a decode step's one token per request, each its own run) take win = 1,
 // one warp pair per token, so that their runs proceed side by side.
+// One bulk copy (TMA) shared -> global, waited for in full, so that the
+// shared source may be reused and the rows are written when the CTA retires.
+__device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
     __nv_bfloat162 r;
     memcpy(&r, &u, 4);
@@ -66,7 +74,18 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
                            : *reinterpret_cast<const uint4*>(rows_new + ((t + r) * num_kv_heads + h) * kHeadDim + c * 8);
     }
 #pragma unroll
-    for (int k = 0; k < kPage / 2; ++k) {
+    // A whole page from offset 0 with its rows staged in shared memory (row
+    // r at byte 256 r: the staging layout is row-major): one bulk store.
+    const bool whole = !FP8 && staged && R == kPage && off == 0;
+    if (whole) {
+        fence_proxy_async_smem();   // this lane's staged rows, for the bulk copy engine
+        __syncwarp();
+        if (lane == 0)
+            bulk_store_s2g(static_cast<__nv_bfloat16*>(pool) + (page * num_kv_heads + h) * kPage * kHeadDim,
+                           smem_addr(staged - lane), kPage * kHeadDim * 2);
+        __syncwarp();
+    }
+    for (int k = 0; k < kPage / 2 && !whole; ++k) {
         const int r = half + 2 * k;
         if (r >= (R + 1) / 2 * 2) break;   // warp-uniform: both half-warps stay for the shuffles
         const bool live = r < R;
@@ -156,7 +175,7 @@ constexpr int kAppendThreads = 128;
 constexpr int64_t kLongAppend = 2048;   // calls of at least this many tokens use 16-token windows
 
 template <bool FP8>
-__global__ void __launch_bounds__(kAppendThreads) append_kv_meta_kernel(
+__global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 8) append_kv_meta_kernel(
     void* __restrict__ k_pool, void* __restrict__ v_pool, __nv_bfloat16* __restrict__ meta,
     float* __restrict__ k_scale, float* __restrict__ v_scale, int64_t num_phys_pages, int num_kv_heads,
     const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
