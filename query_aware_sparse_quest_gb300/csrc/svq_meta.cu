@@ -34,15 +34,17 @@ __device__ __forceinline__ void bulk_store_s2g(void* dst, uint32_t src, uint32_t
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
-__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t u) {
-    __nv_bfloat162 r;
-    memcpy(&r, &u, 4);
-    return r;
+// Lane-wise min / max of two bf16 pairs held in 32-bit words (the
+// instructions behind __hmin2 / __hmax2; bf16 min / max are exact).
+__device__ __forceinline__ uint32_t min_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
-__device__ __forceinline__ uint32_t bits_of(__nv_bfloat162 v) {
-    uint32_t u;
-    memcpy(&u, &v, 4);
-    return u;
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -73,7 +75,6 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
             kw[k] = staged ? staged[32 * k]
                            : *reinterpret_cast<const uint4*>(rows_new + ((t + r) * num_kv_heads + h) * kHeadDim + c * 8);
     }
-#pragma unroll
     // A whole page from offset 0 with its rows staged in shared memory (row
     // r at byte 256 r: the staging layout is row-major): one bulk store.
     const bool whole = !FP8 && staged && R == kPage && off == 0;
@@ -85,7 +86,9 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
                            smem_addr(staged - lane), kPage * kHeadDim * 2);
         __syncwarp();
     }
-    for (int k = 0; k < kPage / 2 && !whole; ++k) {
+#pragma unroll
+    for (int k = 0; k < kPage / 2; ++k) {
+        if (whole) break;
         const int r = half + 2 * k;
         if (r >= (R + 1) / 2 * 2) break;   // warp-uniform: both half-warps stay for the shuffles
         const bool live = r < R;
@@ -124,31 +127,30 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
     }
     if (!is_key) return;
 
-    // The run's key min / max per channel (bf16 min / max are exact).
-    __nv_bfloat162 mn[4], mx[4];
+    // The run's key min / max per channel.
+    uint32_t mn[4], mx[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mn[i] = mx[i] = as_bf162(word_of(kw[0], i));   // row `half` (R >= 2 when half == 1 uses it)
+    for (int i = 0; i < 4; ++i) mn[i] = mx[i] = word_of(kw[0], i);   // row `half` (R >= 2 when half == 1 uses it)
     const bool have = half < R;
 #pragma unroll
     for (int k = 1; k < kPage / 2; ++k) {
         if (half + 2 * k < R) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 v = as_bf162(word_of(kw[k], i));
-                mn[i] = __hmin2(mn[i], v);
-                mx[i] = __hmax2(mx[i], v);
+                mn[i] = min_bf16x2(mn[i], word_of(kw[k], i));
+                mx[i] = max_bf16x2(mx[i], word_of(kw[k], i));
             }
         }
     }
     // Join the half-warps: lane c and lane c + 16 hold the same channels.
+    const bool other_has = (half ^ 1) < R;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const __nv_bfloat162 oa = as_bf162(__shfl_xor_sync(0xffffffffu, bits_of(mn[i]), 16));
-        const __nv_bfloat162 ob = as_bf162(__shfl_xor_sync(0xffffffffu, bits_of(mx[i]), 16));
-        const bool other_has = (half ^ 1) < R;
+        const uint32_t oa = __shfl_xor_sync(0xffffffffu, mn[i], 16);
+        const uint32_t ob = __shfl_xor_sync(0xffffffffu, mx[i], 16);
         if (other_has && have) {
-            mn[i] = __hmin2(mn[i], oa);
-            mx[i] = __hmax2(mx[i], ob);
+            mn[i] = min_bf16x2(mn[i], oa);
+            mx[i] = max_bf16x2(mx[i], ob);
         } else if (other_has) {
             mn[i] = oa;
             mx[i] = ob;
@@ -156,26 +158,23 @@ __device__ __forceinline__ void append_run(void* __restrict__ pool, float* __res
     }
     // Lanes 0-15 write kmin of chunk c, lanes 16-31 kmax of chunk c.
     const bool is_max = half == 1;
-    __nv_bfloat162 acc[4];
+    uint32_t acc[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] = is_max ? mx[i] : mn[i];
     __nv_bfloat16* mdst = meta + ((page * num_kv_heads + h) * 2 + (is_max ? 1 : 0)) * kHeadDim + c * 8;
     if (off > 0) {
         const uint4 w = *reinterpret_cast<const uint4*>(mdst);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 v = as_bf162(word_of(w, i));
-            acc[i] = is_max ? __hmax2(acc[i], v) : __hmin2(acc[i], v);
-        }
+        for (int i = 0; i < 4; ++i) acc[i] = is_max ? max_bf16x2(acc[i], word_of(w, i)) : min_bf16x2(acc[i], word_of(w, i));
     }
-    *reinterpret_cast<uint4*>(mdst) = make_uint4(bits_of(acc[0]), bits_of(acc[1]), bits_of(acc[2]), bits_of(acc[3]));
+    *reinterpret_cast<uint4*>(mdst) = make_uint4(acc[0], acc[1], acc[2], acc[3]);
 }
 
 constexpr int kAppendThreads = 128;
 constexpr int64_t kLongAppend = 2048;   // calls of at least this many tokens use 16-token windows
 
 template <bool FP8>
-__global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 8) append_kv_meta_kernel(
+__global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 7) append_kv_meta_kernel(
     void* __restrict__ k_pool, void* __restrict__ v_pool, __nv_bfloat16* __restrict__ meta,
     float* __restrict__ k_scale, float* __restrict__ v_scale, int64_t num_phys_pages, int num_kv_heads,
     const __nv_bfloat16* __restrict__ k_new, const __nv_bfloat16* __restrict__ v_new,
