@@ -193,10 +193,11 @@ __global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 7) append_kv_meta_ke
     // The slots and new rows are inputs of the call, so they load before the
     // wait for the kernel before (which may still read or write the pool and
     // the metadata): in a chunked prefill a chunk's loads then overlap the
-    // previous chunk's stores.  The rows of a run starting at the window's
-    // first token (a prefill window's only run) go to shared memory by async
-    // copies (lane l: chunk l % 16 of rows l / 16 + 2 k), which hold no
-    // registers; other runs load theirs when they are handled.
+    // previous chunk's stores.  With 16-token windows the rows of a run
+    // starting at the window's first token (a prefill window's only run) go
+    // to shared memory by async copies (lane l: chunk l % 16 of rows
+    // l / 16 + 2 k), which hold no registers; other runs, and every run of a
+    // one-token window (mostly one row long), load theirs when handled.
     __shared__ __align__(16) uint4 s_rows[kAppendThreads / 32][kPage / 2][32];
     uint4* const my_rows = &s_rows[threadIdx.x >> 5][0][lane];
     {
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 7) append_kv_meta_ke
 #pragma unroll
         for (int k = 0; k < kPage / 2; ++k) {
             const int64_t t = t0 + half + 2 * k;
-            const bool ok = active && t < num_tokens;
+            const bool ok = active && win == kPage && t < num_tokens;
             cp_async16(smem_addr(my_rows + 32 * k), ok ? rows_new + (t * num_kv_heads + h) * kHeadDim + c * 8 : rows_new,
                        ok ? 16u : 0u);
         }
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(kAppendThreads, FP8 ? 5 : 7) append_kv_meta_ke
         starts &= starts - 1u;
         const int R = __ffs(~(cont_mask >> (r + 1)));   // 1 + the continuing tokens after r (r + R <= 31)
         append_run<FP8>(is_key ? k_pool : v_pool, is_key ? k_scale : v_scale, meta, is_key, num_kv_heads, h,
-                        rows_new, t0 + r, R, si, r, r == 0 ? my_rows : nullptr);
+                        rows_new, t0 + r, R, si, r, r == 0 && win == kPage ? my_rows : nullptr);
     }
 }
 
