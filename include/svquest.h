@@ -18,6 +18,10 @@
  *    GPU addresses under unified addressing (e.g. from cudaHostAlloc).  Its
  *    kernels then read those inputs and write those results across the
  *    host link themselves, with no separate copy.
+ *  - q, k_new, v_new, out, the pools, the metadata, the fp8 scales and the
+ *    workspaces of sv_sparse_decode(_ex) and sv_quest_decode_step must be
+ *    16-byte aligned (SV_ERR_INVALID_ARG otherwise): kernels move them 16
+ *    bytes at a time.
  *  - bf16 means IEEE bfloat16 stored as 16-bit words.
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls enqueue kernels and return; they never synchronise.

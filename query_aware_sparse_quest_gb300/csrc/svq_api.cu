@@ -159,13 +159,14 @@ int decode_impl(const sv_cache* cache, const void* q, int32_t num_q_heads, const
     if ((st = check_heads(cache, num_q_heads))) return st;
     if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
     if ((st = check_opts(opts))) return st;
-    if (!out || !lse) return SV_ERR_INVALID_ARG;
+    if (!out || !lse || !aligned16(out)) return SV_ERR_INVALID_ARG;
     if (opts->layer < opts->dense_layers) sel_idx = nullptr;   // dense layer: every page
     if (sel_idx && (!sel_cnt || budget_pages < 1)) return SV_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
     const int rows = sel_idx ? rows_per_request(cache, num_q_heads, opts) : cache->num_kv_heads;
     if (static_cast<int64_t>(batch) * rows > 65535) return SV_ERR_UNSUPPORTED;
     if (!workspace) return SV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SV_ERR_INVALID_ARG;   // partials are read 16 bytes at a time
     int sms = 0;
     if ((st = sm_count_of_current_device(&sms))) return st;
     return launch_decode(cache, q, num_q_heads, page_table, seq_lens, batch, max_pages, sel_idx, sel_cnt,
@@ -284,7 +285,7 @@ int step_checks(const sv_cache* cache, const void* q, int32_t num_q_heads, const
     if (st) return st;
     if ((st = check_heads(cache, num_q_heads))) return st;
     if ((st = check_batch(q, page_table, seq_lens, batch, max_pages))) return st;
-    if (!sel_idx || !sel_cnt || !out || !lse || budget_pages < 1) return SV_ERR_INVALID_ARG;
+    if (!sel_idx || !sel_cnt || !out || !lse || budget_pages < 1 || !aligned16(out)) return SV_ERR_INVALID_ARG;
     if (!(softmax_scale > 0.f) || softmax_scale == INFINITY) return SV_ERR_INVALID_ARG;
     if (max_pages > kMaxTopkPages) return SV_ERR_UNSUPPORTED;
     if (static_cast<int64_t>(batch) * cache->num_kv_heads > 65535) return SV_ERR_UNSUPPORTED;
@@ -292,6 +293,7 @@ int step_checks(const sv_cache* cache, const void* q, int32_t num_q_heads, const
         workspace_bytes < sv_quest_decode_step_workspace_size(batch, num_q_heads, cache->num_kv_heads, max_pages,
                                                               budget_pages))
         return SV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SV_ERR_INVALID_ARG;   // a staged query and the partials are read 16 bytes at a time
     return SV_OK;
 }
 }  // namespace

@@ -131,6 +131,9 @@ def test_decode_rejects_bad_args(lib):
     assert call(sel=FAKE, cnt=FAKE, K=0) == SV_ERR_INVALID_ARG
     assert call(ws=None) == SV_ERR_WORKSPACE
     assert call(hq=33) == SV_ERR_INVALID_ARG
+    # out and the workspace are moved 16 bytes at a time
+    assert call(out=ctypes.c_void_p(0x20008)) == SV_ERR_INVALID_ARG
+    assert call(ws=ctypes.c_void_p(0x20004)) == SV_ERR_INVALID_ARG
 
 
 @host_only
@@ -179,6 +182,8 @@ def test_decode_step_rejects_bad_args(lib):
     need = binding.sv_quest_decode_step_workspace_size(8, 32, 4, 100, 16)
     assert call(ws_bytes=need - 1) == SV_ERR_WORKSPACE
     assert call(q=ctypes.c_void_p(0x20002)) == SV_ERR_INVALID_ARG
+    assert call(out=ctypes.c_void_p(0x20008)) == SV_ERR_INVALID_ARG
+    assert call(ws=ctypes.c_void_p(0x20004)) == SV_ERR_INVALID_ARG
 
 
 @host_only
