@@ -325,6 +325,16 @@ def run_gpu(args):
     # before each one (so every step also pays its own launch and events).
     flushed_ms = float(np.mean(timed(g_step.replay, max(3, min(args.steps, 200)))))
     noflush_ms = float(np.mean(timed(g_step.replay, max(3, min(args.steps, 200)), flush_l2=False)))
+    # Ten steps captured in one graph, as an engine that captures a whole
+    # forward pass would run them: each step's scoring kernel then also
+    # follows the previous step's combine by programmatic dependent launch.
+    def ten_steps():
+        for _ in range(10):
+            step()
+
+    g_ten = capture(ten_steps)
+    chained_ms = back_to_back(g_ten.replay, max(3, min(args.steps, 200) // 10)) / 10
+    del g_ten
 
     # ---- per-kernel durations (each call timed alone, same flush discipline)
     n_k = max(3, min(args.steps, 200))
@@ -526,6 +536,7 @@ def run_gpu(args):
                          "see per_step_ms)",
                    "parallelism": f"replicas x{world}"},
         "step_bytes": ab["step"],
+        "chained_10_steps_ms_per_step": round(chained_ms, 5),
         "per_step_ms": {"flushed": round(flushed_ms, 5), "not_flushed": round(noflush_ms, 5),
                         "how": "the same graph replay timed alone between its own pair of events, min(K, 200) "
                                "times, with and without an L2 flush (write one 2xL2 buffer, read another) before "
