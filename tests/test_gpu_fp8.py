@@ -51,9 +51,13 @@ def _decode(dw, sel_idx=None, sel_cnt=None, opts=None):
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-@pytest.mark.parametrize("chunk", [1, 3, 16, 37, 4096])
-def test_fp8_append_bitexact(chunk):
-    spec = synth.SPECS[3].scaled(batch=3, ragged=(20, 700), seed=60 + chunk)
+@pytest.mark.parametrize("chunk,lo,hi", [(1, 20, 700), (3, 20, 700), (16, 20, 700), (37, 20, 700),
+                                         (4096, 20, 700), (4096, 700, 3000), (2048, 700, 3000)])
+def test_fp8_append_bitexact(chunk, lo, hi):
+    """Chunks under 2048 tokens take one-token windows; the longer requests in
+    4096- and 2048-token chunks take 16-token windows (runs starting mid-window,
+    runs cut by a chunk boundary, short last pages)."""
+    spec = synth.SPECS[3].scaled(batch=3 if hi <= 700 else 6, ragged=(lo, hi), seed=60 + chunk + hi)
     wl = synth.make_workload(spec)
     dw = resident.upload(wl, prefill=False, fp8=True)
     host = oracle.Cache(wl.num_phys_pages, spec.num_kv_heads, fp8=True, fill_code=NAN_CODE, fill_scale=float("nan"))

@@ -109,9 +109,18 @@ def pair(cfg):
 
 # ---------------------------------------------------------------- update_meta
 
-@pytest.mark.parametrize("chunk", [1, 3, 16, 37, 4096])
-def test_update_meta_bitexact(chunk):
-    spec = synth.SPECS[3].scaled(batch=3, ragged=(20, 700), seed=30 + chunk)
+# Chunks under 2048 tokens take one-token windows; 4096- and 2048-token chunks
+# of the longer requests take 16-token windows, with runs that start in the
+# middle of a window (request lengths are not multiples of 16), runs cut by a
+# chunk boundary (folded into the stored min / max), whole pages written by
+# one bulk store, and short last pages.
+APPEND_CASES = [(1, 20, 700), (3, 20, 700), (16, 20, 700), (37, 20, 700), (4096, 20, 700),
+                (4096, 700, 3000), (2048, 700, 3000)]
+
+
+@pytest.mark.parametrize("chunk,lo,hi", APPEND_CASES)
+def test_update_meta_bitexact(chunk, lo, hi):
+    spec = synth.SPECS[3].scaled(batch=3 if hi <= 700 else 6, ragged=(lo, hi), seed=30 + chunk + hi)
     wl = synth.make_workload(spec)
     dw = resident.upload(wl, prefill=False)
     host = oracle.Cache(wl.num_phys_pages, spec.num_kv_heads, fill_bits=synth.UNFILLED_BITS)
