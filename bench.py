@@ -608,8 +608,9 @@ def step_bytes(wl, budget_pages, appended=0):
 def run_only(args):
     """One call type alone on the benchmark workload, for profiling with a
     small device footprint (one bf16 or fp8 pool): --only step (the one-call
-    decode step, as a CUDA graph), append (one 4096-token sv_quest_update_meta)
-    or fp8_step (the step over an fp8 pool).  W untimed and K timed calls, each
+    decode step, as a CUDA graph), append (one 4096-token sv_quest_update_meta),
+    fp8_step (the step over an fp8 pool) or fp8_step_budget512 (the fp8 step of
+    16 requests of 65536 tokens at a 512-page budget).  W untimed and K timed calls, each
     after an L2 flush; prints one JSON line with the mean time per call."""
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (no CPU fallback)")
@@ -617,8 +618,10 @@ def run_only(args):
     torch.cuda.set_device(dev)
     build.build()
     spec = synth.SPECS[BENCH_CONFIG]
+    if args.only == "fp8_step_budget512":       # 16 requests of 65536 tokens, K/V-dominated
+        spec = synth.SPECS[4].scaled(budget_pages=512)
     wl = synth.make_workload(spec)
-    dw = resident.upload(wl, device=dev, fp8=args.only == "fp8_step")
+    dw = resident.upload(wl, device=dev, fp8=args.only.startswith("fp8_step"))
     B, Hq, D = dw.q.shape
     Hkv, K = spec.num_kv_heads, spec.budget_pages
     sel_idx, sel_cnt = resident.select_buffers(B, Hkv, K, dev)
@@ -866,7 +869,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--all-configs", action="store_true",
                     help="instead of the benchmark line, one line per workload (step and dense timings)")
-    ap.add_argument("--only", choices=["step", "append", "fp8_step"],
+    ap.add_argument("--only", choices=["step", "append", "fp8_step", "fp8_step_budget512"],
                     help="time one call type alone on the benchmark workload (for profiling), no benchmark line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)     # at least three untimed warm-up steps
