@@ -296,8 +296,11 @@ def run_gpu(args):
     launches_per_step = sum(KERNELS_PER_CALL[c] for c in STEP_CALLS)
     g_step = capture(step)
     g_dense = capture(dense)
+    # Clock sampling starts before the warm-up, so that the timed steps
+    # follow busy GPU work directly (no idle gap in which clocks could drop).
+    sampler = ClockSampler(local_rank)
+    time.sleep(0.25)
     for _ in range(args.warmup):
-        flush.zero_()
         g_step.replay()
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -308,8 +311,6 @@ def run_gpu(args):
     # step reads 198.6 MB of metadata and K/V, more than the 126 MB L2, so
     # nothing of it survives to the next step (the per-step times below,
     # taken with and without a flush, agree).
-    sampler = ClockSampler(local_rank)
-    time.sleep(0.25)
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     for _ in range(args.steps):
