@@ -33,6 +33,13 @@ constexpr int kMaxSplits = 64;
 #define SVQ_DECODE_WAVE_PERMILLE 1000   // split CTAs as a fraction of one full wave
 #endif
 constexpr int kMinPagesPerSplit = 8;
+// Online softmax with a lazily moved base: a head's running base moves only
+// when one of the page's logits exceeds it by more than this many log2 units.
+// Most pages then skip the warp max, the correction factors and the rescale
+// of the 32 output registers; the weights stay at most 2^kRescaleSlack (bf16
+// holds that with room to spare), and sums and outputs share the base, so the
+// result is the same softmax.
+constexpr float kRescaleSlack = 8.f;
 
 struct DecodeArgs {
     int64_t num_phys_pages;
@@ -51,7 +58,7 @@ struct DecodeArgs {
     int num_splits;
     float scale_log2;         // softmax_scale * log2(e)
     float* o_part;            // [B][Hq][S][128] unnormalised partial outputs
-    float2* ml_part;          // [B][Hq][S] (running max in log2 units, sum of exp2)
+    float2* ml_part;          // [B][Hq][S] (base m in log2 units, at most kRescaleSlack below the max; sum of exp2(x - m))
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -279,29 +286,38 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const float x1 = row < valid ? (sa[1] + sb[1]) * a.scale_log2 : -INFINITY;       // token row,   head 2q+1
         const float x2 = row + 8 < valid ? (sa[2] + sb[2]) * a.scale_log2 : -INFINITY;   // token row+8, head 2q
         const float x3 = row + 8 < valid ? (sa[3] + sb[3]) * a.scale_log2 : -INFINITY;   // token row+8, head 2q+1
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+        // The base moves (warp max, correction of sums and outputs) only when
+        // some lane holds a logit more than kRescaleSlack above it.
+        const bool grow = x0 > m_run[0] + kRescaleSlack || x2 > m_run[0] + kRescaleSlack ||
+                          x1 > m_run[1] + kRescaleSlack || x3 > m_run[1] + kRescaleSlack;
+        if (__any_sync(0xffffffffu, grow)) {
+            float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-        for (int s = 4; s < 32; s <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, s));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, s));
+            for (int s = 4; s < 32; s <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, s));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, s));
+            }
+            const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
+            const float alpha0 = fast_exp2(m_run[0] - (mn0 == -INFINITY ? 0.f : mn0));
+            const float alpha1 = fast_exp2(m_run[1] - (mn1 == -INFINITY ? 0.f : mn1));
+            m_run[0] = mn0;
+            m_run[1] = mn1;
+            l_run[0] *= alpha0;
+            l_run[1] *= alpha1;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[mt][0] *= alpha0;
+                o[mt][1] *= alpha1;
+                o[mt][2] *= alpha0;
+                o[mt][3] *= alpha1;
+            }
         }
-        const float mn0 = fmaxf(m_run[0], mx0), mn1 = fmaxf(m_run[1], mx1);
-        const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-        const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-        const float alpha0 = fast_exp2(m_run[0] - base0), alpha1 = fast_exp2(m_run[1] - base1);
+        const float base0 = m_run[0] == -INFINITY ? 0.f : m_run[0];
+        const float base1 = m_run[1] == -INFINITY ? 0.f : m_run[1];
         const float p0 = fast_exp2(x0 - base0), p1 = fast_exp2(x1 - base1);
         const float p2 = fast_exp2(x2 - base0), p3 = fast_exp2(x3 - base1);
-        m_run[0] = mn0;
-        m_run[1] = mn1;
-        l_run[0] = l_run[0] * alpha0 + p0 + p2;
-        l_run[1] = l_run[1] * alpha1 + p1 + p3;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            o[mt][0] *= alpha0;
-            o[mt][1] *= alpha1;
-            o[mt][2] *= alpha0;
-            o[mt][3] *= alpha1;
-        }
+        l_run[0] += p0 + p2;
+        l_run[1] += p1 + p3;
 
         // P^T as the B operand: lane needs P[token 2 quad + {0,1} (+8)][head row].
         const uint32_t lo = pack_bf16x2(p0, p1);   // token row:   heads 2q, 2q+1

@@ -4,12 +4,12 @@
 // attention backend) with K and V rows stored as e4m3 codes and one fp32
 // scale per (token, kv head) row.
 //
-// Per CTA: one producer warp and four consumer warps over a 16-stage ring.  A
+// Per CTA: one producer warp and four consumer warps over an 8-stage ring.  A
 // stage holds one page of one kv head: the K tile and the V tile, each a
 // 16 x 128-byte TMA box with the 128-byte swizzle (2 KB), plus the page's 16
 // K scales and 16 V scales (128 B, bulk copies) in a separate scale ring.
-// Producer lanes 2u and 2u+1 feed stage u (K, V): the pages whose list
-// position is u mod 16, each pair on its own.
+// Producer lanes 4u and 4u+1 feed stage u (K, V): the pages whose list
+// position is u mod 8, each lane group on its own.
 //
 // The tensor cores read the codes without a staging pass.  e4m3 values are
 // exact in f16, so codes convert to f16 pairs (cvt e4m3x2 -> f16x2) and feed
@@ -38,13 +38,19 @@ SVQ_DEFINE_ERROR_WORD(read_error_decode_fp8)
 constexpr int kF8Consumers = 4;
 constexpr int kF8Threads = (kF8Consumers + 1) * 32;
 constexpr int kF8Producer = kF8Consumers;
-constexpr int kF8Stages = 16;                    // pages in flight per CTA; lanes 2u, 2u+1 feed stage u
+// Pages in flight per CTA.  Eight stages (34 KB of shared memory) let four
+// CTAs share an SM, which the registers allow: sixteen consumer warps per SM
+// and finer splits; sixteen stages left room for three.
+constexpr int kF8Stages = 8;
+constexpr int kF8LanesPerStage = 32 / kF8Stages; // producer lanes per stage: the first moves K, the second V
 constexpr int kF8Box = kPage * kHeadDim;         // 16 rows x 128 e4m3 = 2 KB
 constexpr int kF8Stage = 2 * kF8Box;             // K box | V box
 constexpr int kF8ScaleBytes = 2 * kPage * 4;     // 16 K scales | 16 V scales
 constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Stages * kF8ScaleBytes;
 static_assert(kF8Stages % kF8Consumers == 0, "each ring stage must belong to one consumer warp");
-static_assert(2 * kF8Stages == 32, "two producer lanes per stage");
+static_assert(32 % kF8Stages == 0 && kF8LanesPerStage >= 2, "at least two producer lanes per stage");
+static_assert(kF8Stages * kF8Stage >= (kF8Consumers * kMaxGroup * kHeadDim + 2 * kF8Consumers * kMaxGroup) * 4,
+              "the warps merge through the ring");
 
 struct DecodeF8Args {
     int64_t num_phys_pages;
@@ -148,11 +154,12 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const int chunk = (count + a.num_splits - 1) / a.num_splits;
         const int j0 = min(count, split * chunk);
         const int my_count = min(count, j0 + chunk) - j0;
-        const int u = lane >> 1, part = lane & 1;   // stage u; part 0 moves K, part 1 moves V
+        const int u = lane / kF8LanesPerStage, part = lane % kF8LanesPerStage;   // stage u; part 0 moves K, part 1 V
+        const bool mover = part < 2;
         const uint32_t fb = full0 + u * 8;
         const uint32_t eb = empty0 + u * 8;
-        const void* tmap = part ? static_cast<const void*>(&tmap_v) : static_cast<const void*>(&tmap_k);
-        const float* scale_src = part ? a.v_scale : a.k_scale;
+        const void* tmap = part == 1 ? static_cast<const void*>(&tmap_v) : static_cast<const void*>(&tmap_k);
+        const float* scale_src = part == 1 ? a.v_scale : a.k_scale;
         // Lane l resolves list position base + l to (physical page, valid
         // tokens); the next 32 are resolved while the current 32 are issued.
         auto resolve = [&](int base, int& phys_out, int& valid_out) {
@@ -181,12 +188,12 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         for (int base = 0; base < my_count && ok; base += 32) {
             resolve(base + 32, nxt_phys, nxt_valid);
             for (int sub = 0; sub < 32 && base + sub < my_count; sub += kF8Stages) {
-                // Lane pair u issues list position i = base + sub + u into stage u.
+                // Lane group u issues list position i = base + sub + u into stage u.
                 const int i = base + sub + u;
                 const int phys = __shfl_sync(0xffffffffu, cur_phys, sub + u);
                 const int valid = __shfl_sync(0xffffffffu, cur_valid, sub + u);
                 bool mine_ok = true;
-                if (i < my_count) {
+                if (mover && i < my_count) {
                     if (i >= kF8Stages) mine_ok = mbar_wait_bounded(eb, ((i / kF8Stages) - 1) & 1);
                     if (mine_ok) {
                         if (part == 0) {
