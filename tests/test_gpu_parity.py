@@ -7,6 +7,8 @@ within max-abs 2e-2 of the oracle's fp32 outputs; fp32 lse within 1e-3.
 """
 from __future__ import annotations
 
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -271,7 +273,6 @@ def test_short_and_ragged_requests():
 
 def _with_lengths(spec, lens):
     """A workload of `spec` whose requests have exactly the lengths `lens`."""
-    import dataclasses
     lo = int(lens.min())
     base = synth.make_workload(spec.scaled(batch=len(lens), ragged=(int(lens.max()), int(lens.max()))))
     # Truncate each request of the max-length stream to its own length.
@@ -318,6 +319,39 @@ def test_nan_in_unfilled_slots_is_masked():
     for s_, c_ in ((sel, cnt), (None, None)):
         out, lse = gpu_decode(dw, s_, c_)
         assert np.isfinite(out).all() and np.isfinite(lse).all()
+        check_attention(out, lse, *oracle.decode(host, wl.q, wl.page_table, wl.seq_lens, s_, c_))
+
+
+@pytest.mark.parametrize("slope", [3.0, 12.0])
+def test_logits_rising_across_pages(slope):
+    """Keys move along the query group's direction page after page, so the
+    logits of the group's heads rise by about `slope` log2 units per page up to
+    the last page (which keeps its own keys): at 12 the split kernel's running
+    softmax base moves on every page, at 3 every few pages, with weights up to
+    the 2^8 that the lazily moved base allows in between."""
+    spec = synth.SPECS[1].scaled(batch=2, ctx=16 * 60 + 7, budget_pages=24)
+    wl = synth.make_workload(spec)
+    Hkv, Hq, P = spec.num_kv_heads, spec.num_q_heads, spec.page_size
+    G = Hq // Hkv
+    q = bf16_bits_to_f32(wl.q).astype(np.float64)
+    k = bf16_bits_to_f32(wl.k_tok).astype(np.float64)
+    scale_log2 = np.log2(np.e) / np.sqrt(spec.head_dim)
+    off = 0
+    for b, L in enumerate(wl.seq_lens):
+        page = np.arange(int(L)) // P
+        for g in range(Hkv):
+            u = q[b, g * G:(g + 1) * G].sum(axis=0)
+            step = slope / (scale_log2 * (u @ u) / G)   # u.(step u) / G heads ~ slope log2 units per head
+            k[off:off + int(L), g] += np.outer(page - page[-1], step * u)
+        off += int(L)
+    wl = dataclasses.replace(wl, k_tok=synth.to_bf16_bits(k.astype(np.float32)))
+    dw = resident.upload(wl)
+    host = oracle.build_cache(wl, synth.UNFILLED_BITS)
+    sel, cnt, _ = gpu_select(dw, spec.budget_pages, use_workspace=False)
+    ref_sel, ref_cnt, ref_scores = oracle.select(host, wl.q, wl.page_table, wl.seq_lens, spec.budget_pages)
+    check_selection(sel, cnt, ref_sel, ref_cnt, ref_scores, n_pages_of(wl))
+    for s_, c_ in ((sel, cnt), (None, None)):
+        out, lse = gpu_decode(dw, s_, c_)
         check_attention(out, lse, *oracle.decode(host, wl.q, wl.page_table, wl.seq_lens, s_, c_))
 
 
