@@ -398,6 +398,35 @@ def run_gpu(args):
     fp8_same_sel = bool(torch.equal(cnt8, sel_cnt))
     del dw8, g_step8
 
+    # ---- the selection options on the same workload: sv_quest_select_ex +
+    # sv_sparse_decode_ex as one CUDA graph, timed back to back like the
+    # headline.  Forced pages (the first page and the last four, counted in the
+    # budget) and one page set per query head (each of the 32 query heads reads
+    # its own 256 pages of its kv head).
+    n_pages = (wl.seq_lens.astype(np.int64) + spec.page_size - 1) // spec.page_size
+    variants = {"note": "select_ex + decode_ex as one graph, back to back; bytes = metadata + the K/V of every "
+                        "selection row + page table + q / out / lse"}
+    for vname, vopts, rows in (("sink1_window4", binding.quest_opts(sink_pages=1, window_pages=4), Hkv),
+                               ("per_q_head", binding.quest_opts(per_q_head=True), Hq)):
+        sv, cv = resident.select_buffers(B, rows, K, dev)
+        wsv = resident.workspace(binding.sv_quest_select_ex_workspace_size(B, Hq, Hkv, max_pages, vopts), dev)
+
+        def var_step(vopts=vopts, sv=sv, cv=cv, wsv=wsv):
+            binding.sv_quest_select_ex(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, vopts, sv, cv, workspace=wsv)
+            binding.sv_sparse_decode_ex(dw.cache, dw.q, dw.page_table, dw.seq_lens, sv, cv, vopts, out, lse, ws)
+
+        for _ in range(3):
+            var_step()
+        gv = capture(var_step)
+        tv = back_to_back(gv.replay, max(3, min(args.steps, 200)))
+        vbytes = (int(n_pages.sum()) * Hkv * 2 * D * 2                                 # metadata
+                  + int(np.minimum(n_pages, K).sum()) * rows * spec.page_size * D * 2 * 2   # K/V per row
+                  + int(n_pages.sum()) * 4 + B * Hq * (D * 2 + D * 2 + 4))           # page table, q, out, lse
+        variants[vname] = {"ms_per_step": round(tv, 5), "steps_per_s": round(1e3 / tv, 2), "bytes": vbytes,
+                           "gbs": round(vbytes / (tv * 1e-3) / 1e9, 1), "selection_rows_per_request": rows}
+        del gv, sv, cv, wsv
+    torch.cuda.synchronize(dev)
+
     # ---- where selected K/V bytes dominate: 16 requests of 65536 tokens at a
     # 512-page budget, the step over a bf16 and over an fp8 pool (each a CUDA
     # graph, timed back to back), and each sparse decode alone (L2 flushed).
@@ -579,6 +608,7 @@ def run_gpu(args):
                                "how": "request 0's tokens in 4096-token chunks, one sv_quest_update_meta per "
                                       "chunk, all chunks one CUDA graph"}},
         "kv_heavy_budget512": kv_heavy,
+        "quest_variants": variants,
         "gpu_launches": launches_per_step * args.steps,
         "launches_per_step": launches_per_step,
         "gpu_launches_source": "kernels per call (sv_quest_decode_step: score 1 + top-K 1 + split decode 1 + combine 1), "

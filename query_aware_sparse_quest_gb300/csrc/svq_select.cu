@@ -479,7 +479,9 @@ int launch_score(const sv_cache* c, const void* q, int num_q_heads, const int32_
 // threshold search is a selection, not a sort:
 //  1. one histogram over [min key, max key] in 2048 power-of-two-wide bins
 //     (a bin index is a right shift of key - min, so bins are monotone in the
-//     score) locates the bin b* holding the K-th best key;
+//     score) locates the bin b* holding the K-th best key; forced pages (+inf)
+//     stay out of the max and join the top bin, so that a few of them do not
+//     squeeze every scored page into a handful of bins;
 //  2. if b* holds few keys (<= kCandCap), each of them gets its exact rank in
 //     (key desc, page asc) order by comparing against the others, which gives
 //     the threshold key T and how many keys equal to T are taken;
@@ -604,6 +606,9 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
 #pragma unroll
         for (int e = 0; e < ITEMS; ++e) f[e] = i0 + e < n ? row[i0 + e] : 0.f;
     }
+    // Forced pages score +inf; they stay out of the maximum, so that the
+    // histogram spans the scored pages, and land in the top bin.
+    constexpr uint32_t kForcedKey = 0xff800000u;   // order_key(+inf)
     uint32_t key[ITEMS];
     uint32_t lo = 0xffffffffu, hi = 0u;
 #pragma unroll
@@ -611,7 +616,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         key[e] = order_key(f[e]);
         if (i0 + e < n) {
             lo = min(lo, key[e]);
-            hi = max(hi, key[e]);
+            if (key[e] != kForcedKey) hi = max(hi, key[e]);
         }
     }
     lo = __reduce_min_sync(0xffffffffu, lo);
@@ -624,14 +629,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
     // Every warp folds the per-warp values itself (no second barrier).
     lo = __reduce_min_sync(0xffffffffu, lane < kTopkWarps ? warp_lo[lane] : 0xffffffffu);
     hi = __reduce_max_sync(0xffffffffu, lane < kTopkWarps ? warp_hi[lane] : 0u);
+    hi = max(hi, lo);   // every page forced
     const uint32_t range = hi - lo;
     const int range_bits = range == 0 ? 0 : 32 - __clz(range);            // range < 2^bits
     const uint32_t shift = range_bits > 11 ? range_bits - 11 : 0;        // (range >> shift) < 2048
+    // Bins are monotone in the key; keys above hi (forced pages) join the top bin.
+    auto bin_of = [&](uint32_t k) { return min((k - lo) >> shift, static_cast<uint32_t>(kRadixBins - 1)); };
 
-    // 2. histogram of (key - lo) >> shift; bin of the m-th best key.
+    // 2. histogram of the bins; bin of the m-th best key.
 #pragma unroll
     for (int e = 0; e < ITEMS; ++e)
-        if (i0 + e < n) atomicAdd(&hist[(key[e] - lo) >> shift], 1u);
+        if (i0 + e < n) atomicAdd(&hist[bin_of(key[e])], 1u);
     __syncthreads();
     find_bin_from_top(hist, static_cast<uint32_t>(m), warp_tot, &s_bin, &s_rem);
     const uint32_t bstar = s_bin, need = s_rem;
@@ -640,7 +648,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_pages_kernel(const float* _
         // 3a. exact rank of each key of bin b* among the others.
 #pragma unroll
         for (int e = 0; e < ITEMS; ++e) {
-            if (i0 + e < n && ((key[e] - lo) >> shift) == bstar) {
+            if (i0 + e < n && bin_of(key[e]) == bstar) {
                 const uint32_t pos = atomicAdd(&s_cand, 1u);
                 cand_key[pos] = key[e];
                 cand_idx[pos] = i0 + e;

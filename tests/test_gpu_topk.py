@@ -103,3 +103,20 @@ def test_topk_short_rows_and_large_budgets():
     scores = rng.standard_normal((len(seq_lens), 2, 3001))
     for K in (1, 100, 256, 257, 4096):
         check(scores, seq_lens, K)
+
+
+@pytest.mark.parametrize("K", [1, 3, 5, 37, 256])
+def test_topk_forced_pages_at_both_ends(K):
+    """Forced pages (the first page and the last four of each row) score +inf,
+    as the scoring kernel writes them: they rank above every scored page, among
+    themselves by lower page index, and the histogram still spans the scored
+    pages.  Budgets below, at and above the five forced pages."""
+    rng = np.random.default_rng(500 + K)
+    B, R, mp = 3, 4, 8000
+    seq_lens = np.array([mp * PAGE, mp * PAGE - 7, 5000 * PAGE + 1])
+    scores = rng.standard_normal((B, R, mp))
+    n = -(-seq_lens // PAGE)
+    for b in range(B):
+        scores[b, :, 0] = np.inf
+        scores[b, :, n[b] - 4:n[b]] = np.inf
+    check(scores, seq_lens, K)
