@@ -151,6 +151,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
         const int j0 = min(count, split * chunk);
         const int my_count = min(count, j0 + chunk) - j0;
         const int u = lane >> 2, box = lane & 3;   // lane group u owns stage u
+        const uint64_t policy = l2_evict_first_policy();
         const uint32_t fb = full0 + u * 8;
         const uint32_t eb = empty0 + u * 8;
         const void* tmap = box < 2 ? static_cast<const void*>(&tmap_k) : static_cast<const void*>(&tmap_v);
@@ -199,7 +200,7 @@ __global__ void __launch_bounds__(kDecodeThreads) flash_decode_split_kernel(cons
                         }
                         if (phys >= 0 && mover) {
                             const int y = static_cast<int>((static_cast<int64_t>(phys) * a.num_kv_heads + kvh) * kPage);
-                            tma_load_3d(dst, tmap, 0, y, 0, fb);
+                            tma_load_3d_hint(dst, tmap, 0, y, 0, fb, policy);
                         }
                         last = i;
                     }

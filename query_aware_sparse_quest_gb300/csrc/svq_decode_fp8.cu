@@ -155,6 +155,7 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const int j0 = min(count, split * chunk);
         const int my_count = min(count, j0 + chunk) - j0;
         const int u = lane / kF8LanesPerStage, part = lane % kF8LanesPerStage;   // stage u; part 0 moves K, part 1 V
+        const uint64_t policy = l2_evict_first_policy();
         const bool mover = part < 2;
         const uint32_t fb = full0 + u * 8;
         const uint32_t eb = empty0 + u * 8;
@@ -203,10 +204,10 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
                         }
                         if (phys >= 0) {
                             const int64_t head_row = static_cast<int64_t>(phys) * a.num_kv_heads + kvh;
-                            tma_load_2d(ring_s + u * kF8Stage + part * kF8Box, tmap, 0,
-                                        static_cast<int>(head_row * kPage), fb);
-                            bulk_copy_g2s(scale_s + u * kF8ScaleBytes + part * (kPage * 4),
-                                          scale_src + head_row * kPage, kPage * 4, fb);
+                            tma_load_2d_hint(ring_s + u * kF8Stage + part * kF8Box, tmap, 0,
+                                             static_cast<int>(head_row * kPage), fb, policy);
+                            bulk_copy_g2s_hint(scale_s + u * kF8ScaleBytes + part * (kPage * 4),
+                                               scale_src + head_row * kPage, kPage * 4, fb, policy);
                         }
                         last = i;
                     }

@@ -284,6 +284,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
         const uint32_t ring_s = smem_addr(ring);
         int issued_last = -1;   // highest page this lane issued
         bool failed = false;
+        const uint64_t policy = l2_evict_first_policy();
         for (int p = lane; p < span; p += 32) {
             const int phys = nxt;
             if (p + 32 < span) nxt = pt_row[p + 32];
@@ -297,8 +298,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1) score_pages_kernel(
             slot_ok[slot] = ok ? 1 : 0;
             if (ok) {
                 mbar_arrive_expect_tx(fb, S::kPageBytes);
-                bulk_copy_g2s(ring_s + slot * S::kPageBytes, meta_bytes + static_cast<int64_t>(phys) * S::kPageBytes,
-                              S::kPageBytes, fb);
+                bulk_copy_g2s_hint(ring_s + slot * S::kPageBytes,
+                                   meta_bytes + static_cast<int64_t>(phys) * S::kPageBytes, S::kPageBytes, fb, policy);
             } else {
                 svq_flag(SV_DEVERR_PAGE_TABLE);
                 mbar_arrive(fb);
