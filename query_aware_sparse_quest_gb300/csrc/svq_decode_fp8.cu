@@ -20,10 +20,13 @@
 //    channels as (2q, 2q+1) -> (4q, 4q+1) and (2q+8, 2q+9) -> (4q+2, 4q+3); a
 //    dot product does not depend on the channel order, so the q fragments
 //    (B operand) use the same map.
-//  - V as the A operand of O^T += V^T P^T: ldmatrix.trans on the byte tile
-//    hands lane (g, q) channels 2g, 2g+1 of tokens 2q, 2q+1; byte permutes
-//    split them into an even-channel and an odd-channel fragment, i.e. two
-//    MMAs whose output rows are channels 2g (+16) and 2g+1 (+16) of the block.
+//  - V as the A operand of O^T += V^T P^T: the transposing byte ldmatrix
+//    (m16n16 .b8) hands lane (g, q) tokens 4q .. 4q+3 of channels g and g + 8
+//    of a 16-channel block, two tokens of one channel per 16-bit half, which
+//    is what the pairwise conversion takes; the MMA's k slots (2q, 2q+1) and
+//    (2q+8, 2q+9) are then tokens (4q, 4q+1) and (4q+2, 4q+3).  The logit
+//    tile's rows are permuted to match (token_of_row), so that the weights
+//    reach their B-operand lanes through the same four shuffles.
 // Scales: the logit of token t is s_k(t) * (q . codes_t); the value weight of
 // token t is p_t * s_v(t) (the softmax sum uses p_t).
 #include <cuda.h>
@@ -87,8 +90,23 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
 __device__ __forceinline__ uint32_t swz8(int row, int chunk) {
     return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
+// Token held by row m of the S^T = K Q^T tile.  The value MMA reads tokens
+// 4q .. 4q+3 as its k slots (2q, 2q+1, 2q+8, 2q+9), so the logit tile puts
+// tokens 4q, 4q+1 in rows 2q, 2q+1 and tokens 4q+2, 4q+3 in rows 2q+8, 2q+9:
+// the weights then reach their B-operand lanes through the usual shuffles.
+__device__ __forceinline__ int token_of_row(int m) { return 4 * ((m & 7) >> 1) + (m & 1) + 2 * (m >> 3); }
+// Two 16 x 16 byte tiles transposed: lane 4c + j receives bytes (rows 4j .. 4j+3,
+// column c) in r0 and (rows 4j .. 4j+3, column c + 8) in r1 of tile 0, and the
+// same of tile 1 in r2, r3.  Lanes 0-15 address tile 0's rows, lanes 16-31
+// tile 1's.
+__device__ __forceinline__ void ldmatrix_b8_x2_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                     uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m16n16.x2.trans.shared.b8 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
 
-__global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __grid_constant__ DecodeF8Args a,
+__global__ void __launch_bounds__(kF8Threads, 4) flash_decode_fp8_kernel(const __grid_constant__ DecodeF8Args a,
                                                                     const __grid_constant__ CUtensorMap tmap_k,
                                                                     const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ unsigned char smem_raw[];
@@ -253,16 +271,15 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
     const int j0 = min(count, split * chunk);
     const int my_count = min(count, j0 + chunk) - j0;
 
-    float o[8][4];   // o[2 cb + parity]: output channels 32 cb + 2 r + parity (+16 for rows r + 8)
+    float o[8][4];   // o[mt]: output channels 16 mt + r (and + 8), heads 2 quad, 2 quad + 1
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
     float m_run[2] = {-INFINITY, -INFINITY};
     float l_run[2] = {0.f, 0.f};
     const int mat = lane >> 3, r8 = lane & 7;
-    const int krow = r8 + 8 * (mat & 1);        // K: matrices (rows 0-7 | 8-15) x (chunk 2kp | 2kp+1)
+    const int ktok = token_of_row(r8 + 8 * (mat & 1));   // K: matrices (rows 0-7 | 8-15) x (chunk 2kp | 2kp+1)
     const int kchunk_off = mat >> 1;
-    const int vrow = r8 + 8 * (mat >> 1);       // V (trans): matrices (chunk 2cb | 2cb+1) x (tokens 0-7 | 8-15)
-    const int vchunk_off = mat & 1;
+    const int tok0 = token_of_row(row), tok1 = token_of_row(row + 8);   // tokens of this lane's logits
     for (int i = warp; i < my_count; i += kF8Consumers) {
         const int stage = i % kF8Stages;
         const bool okw = mbar_wait_bounded(full0 + stage * 8, (i / kF8Stages) & 1);
@@ -291,18 +308,18 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
             uint32_t r0, r1, r2, r3;
-            ldmatrix_x4(st_s + swz8(krow, 2 * kp + kchunk_off), r0, r1, r2, r3);
+            ldmatrix_x4(st_s + swz8(ktok, 2 * kp + kchunk_off), r0, r1, r2, r3);
             mma_f16_16816(sa, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
                           e4m3x2_to_f16x2(r1 >> 16), qf[2 * kp][0], qf[2 * kp][1]);
             mma_f16_16816(sb, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
                           e4m3x2_to_f16x2(r3 >> 16), qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
         }
-        const bool v0 = row < valid, v1 = row + 8 < valid;
-        const float ks0 = v0 ? ks[row] : 0.f, ks1 = v1 ? ks[row + 8] : 0.f;
-        const float x0 = v0 ? (sa[0] + sb[0]) * ks0 * a.scale_log2 : -INFINITY;   // token row,   head 2q
-        const float x1 = v0 ? (sa[1] + sb[1]) * ks0 * a.scale_log2 : -INFINITY;   // token row,   head 2q+1
-        const float x2 = v1 ? (sa[2] + sb[2]) * ks1 * a.scale_log2 : -INFINITY;   // token row+8, head 2q
-        const float x3 = v1 ? (sa[3] + sb[3]) * ks1 * a.scale_log2 : -INFINITY;   // token row+8, head 2q+1
+        const bool v0 = tok0 < valid, v1 = tok1 < valid;
+        const float ks0 = v0 ? ks[tok0] : 0.f, ks1 = v1 ? ks[tok1] : 0.f;
+        const float x0 = v0 ? (sa[0] + sb[0]) * ks0 * a.scale_log2 : -INFINITY;   // token tok0, head 2q
+        const float x1 = v0 ? (sa[1] + sb[1]) * ks0 * a.scale_log2 : -INFINITY;   // token tok0, head 2q+1
+        const float x2 = v1 ? (sa[2] + sb[2]) * ks1 * a.scale_log2 : -INFINITY;   // token tok1, head 2q
+        const float x3 = v1 ? (sa[3] + sb[3]) * ks1 * a.scale_log2 : -INFINITY;   // token tok1, head 2q+1
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int s = 4; s < 32; s <<= 1) {
@@ -326,10 +343,12 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
             o[mt][2] *= alpha0;
             o[mt][3] *= alpha1;
         }
-        // Value weights p_t * s_v(t) as P^T (tokens x heads, f16).
-        const float vs0 = v0 ? vs[row] : 0.f, vs1 = v1 ? vs[row + 8] : 0.f;
-        const uint32_t lo = pack_half2(p0 * vs0, p1 * vs0);   // token row:   heads 2q, 2q+1
-        const uint32_t hi = pack_half2(p2 * vs1, p3 * vs1);   // token row+8: heads 2q, 2q+1
+        // Value weights p_t * s_v(t) as P^T (k slots x heads, f16): lane (g, q)
+        // needs tokens 4q, 4q+1 (slots 2q, 2q+1) and 4q+2, 4q+3 (slots 2q+8,
+        // 2q+9) of head g, held by the lanes of rows 2q and 2q+1.
+        const float vs0 = v0 ? vs[tok0] : 0.f, vs1 = v1 ? vs[tok1] : 0.f;
+        const uint32_t lo = pack_half2(p0 * vs0, p1 * vs0);   // token tok0: heads 2q, 2q+1
+        const uint32_t hi = pack_half2(p2 * vs1, p3 * vs1);   // token tok1: heads 2q, 2q+1
         const int src0 = (2 * quad) * 4 + (row >> 1);
         const int src1 = (2 * quad + 1) * 4 + (row >> 1);
         const uint32_t lo0 = __shfl_sync(0xffffffffu, lo, src0);
@@ -340,17 +359,17 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const uint32_t pb0 = __byte_perm(lo0, lo1, selector);
         const uint32_t pb1 = __byte_perm(hi0, hi1, selector);
 
-        // O^T += V^T P^T, 32 channels per ldmatrix.trans: even and odd channels.
+        // O^T += V^T P^T, 32 channels per transposing byte ldmatrix: lane
+        // (g, q) gets tokens 4q .. 4q+3 of channels 16 mt + g and 16 mt + g + 8,
+        // two tokens of one channel per 16-bit half, as the conversion wants.
 #pragma unroll
         for (int cb = 0; cb < 4; ++cb) {
             uint32_t r0, r1, r2, r3;
-            ldmatrix_x4_trans(st_s + kF8Box + swz8(vrow, 2 * cb + vchunk_off), r0, r1, r2, r3);
-            mma_f16_16816(o[2 * cb], e4m3x2_to_f16x2(__byte_perm(r0, 0u, 0x0020u)),
-                          e4m3x2_to_f16x2(__byte_perm(r1, 0u, 0x0020u)), e4m3x2_to_f16x2(__byte_perm(r2, 0u, 0x0020u)),
-                          e4m3x2_to_f16x2(__byte_perm(r3, 0u, 0x0020u)), pb0, pb1);
-            mma_f16_16816(o[2 * cb + 1], e4m3x2_to_f16x2(__byte_perm(r0, 0u, 0x0031u)),
-                          e4m3x2_to_f16x2(__byte_perm(r1, 0u, 0x0031u)), e4m3x2_to_f16x2(__byte_perm(r2, 0u, 0x0031u)),
-                          e4m3x2_to_f16x2(__byte_perm(r3, 0u, 0x0031u)), pb0, pb1);
+            ldmatrix_b8_x2_trans(st_s + kF8Box + swz8(lane & 15, 2 * cb + (lane >> 4)), r0, r1, r2, r3);
+            mma_f16_16816(o[2 * cb], e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1), e4m3x2_to_f16x2(r0 >> 16),
+                          e4m3x2_to_f16x2(r1 >> 16), pb0, pb1);
+            mma_f16_16816(o[2 * cb + 1], e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3), e4m3x2_to_f16x2(r2 >> 16),
+                          e4m3x2_to_f16x2(r3 >> 16), pb0, pb1);
         }
         __syncwarp();   // every lane has read the stage before it is released
         if (lane == 0) mbar_arrive(empty0 + stage * 8);
@@ -373,11 +392,11 @@ __global__ void __launch_bounds__(kF8Threads) flash_decode_fp8_kernel(const __gr
         const int h0 = 2 * quad, h1 = 2 * quad + 1;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            const int ch = 32 * (mt >> 1) + 2 * row + (mt & 1);
+            const int ch = 16 * mt + row;
             ow[h0 * kHeadDim + ch] = o[mt][0];
             ow[h1 * kHeadDim + ch] = o[mt][1];
-            ow[h0 * kHeadDim + ch + 16] = o[mt][2];
-            ow[h1 * kHeadDim + ch + 16] = o[mt][3];
+            ow[h0 * kHeadDim + ch + 8] = o[mt][2];
+            ow[h1 * kHeadDim + ch + 8] = o[mt][3];
         }
         if (row == 0) {
             sm_m[warp * kMaxGroup + h0] = m_run[0];
