@@ -120,6 +120,32 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+class Sections:
+    """NVTX ranges around the benchmark's sections (host-side markers, so that
+    an ncu capture can be limited to one with --nvtx --nvtx-include <name>/);
+    a no-op where NVTX is unavailable."""
+
+    def __init__(self):
+        self.open = False
+        try:
+            self.nvtx = torch.cuda.nvtx
+            self.nvtx.range_push("probe")
+            self.nvtx.range_pop()
+        except Exception:
+            self.nvtx = None
+
+    def __call__(self, name: str):
+        self.close()
+        if self.nvtx is not None:
+            self.nvtx.range_push(name)
+            self.open = True
+
+    def close(self):
+        if self.open:
+            self.nvtx.range_pop()
+            self.open = False
+
+
 def kernel_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel source (else None)."""
@@ -309,13 +335,17 @@ def run_gpu(args):
     # ---- timed region: K steps back to back (one graph replay per step)
     # between one pair of events.  L2 is not flushed between steps: each
     # step reads 198.6 MB of metadata and K/V, more than the 126 MB L2, so
-    # nothing of it survives to the next step (the per-step times below,
-    # taken with and without a flush, agree).
+    # none of it survives to the next step (the per-step times below, taken
+    # with and without a flush, differ only by the small structures the
+    # kernels reuse: page table, scores, selection lists).
+    mark = Sections()
+    mark("headline_steps")
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
     for _ in range(args.steps):
         g_step.replay()
     e_end.record(stream)
+    mark.close()
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
@@ -324,6 +354,7 @@ def run_gpu(args):
     ms_per_step = total_ms / args.steps
     # The same step timed alone: events around each replay, L2 flushed
     # before each one (so every step also pays its own launch and events).
+    mark("step_alone")
     flushed_ms = float(np.mean(timed(g_step.replay, max(3, min(args.steps, 200)))))
     noflush_ms = float(np.mean(timed(g_step.replay, max(3, min(args.steps, 200)), flush_l2=False)))
     # Ten steps captured in one graph, as an engine that captures a whole
@@ -338,18 +369,21 @@ def run_gpu(args):
     del g_ten
 
     # ---- per-kernel durations (each call timed alone, same flush discipline)
+    mark("per_kernel")
     n_k = max(3, min(args.steps, 200))
     t_score = float(np.mean(timed(score, n_k)))
     t_topk = float(np.mean(timed(topk, n_k)))
     t_dec = float(np.mean(timed(decode, n_k)))
 
     # ---- dense (all pages) comparator
+    mark("dense")
     dense_ms = float(np.mean(timed(g_dense.replay, max(3, min(args.steps, 50)))))
 
     step()   # the step again (the dense comparator overwrote out / lse)
     torch.cuda.synchronize(dev)
 
     # ---- bulk prefill append: one 4096-token chunk through sv_quest_update_meta
+    mark("prefill_append")
     # (request 0's first 4096 tokens rewritten into their own slots: same pool)
     T = min(4096, int(wl.seq_lens[0]))
     k_new = resident.bf16_tensor(wl.k_tok[:T], dev)
@@ -380,6 +414,7 @@ def run_gpu(args):
     del k_all, v_all, slots_all, g_prefill
 
     # ---- the same step over an fp8 (e4m3) pool of the same tokens
+    mark("fp8_step")
     dw8 = resident.upload(wl, device=dev, fp8=True)
     sel8, cnt8 = resident.select_buffers(B, Hkv, K, dev)
     out8, lse8 = torch.empty_like(out), torch.empty_like(lse)
@@ -398,6 +433,7 @@ def run_gpu(args):
     fp8_same_sel = bool(torch.equal(cnt8, sel_cnt))
     del dw8, g_step8
 
+    mark("quest_variants")
     # ---- the selection options on the same workload: sv_quest_select_ex +
     # sv_sparse_decode_ex as one CUDA graph, timed back to back like the
     # headline.  Forced pages (the first page and the last four, counted in the
@@ -427,6 +463,7 @@ def run_gpu(args):
         del gv, sv, cv, wsv
     torch.cuda.synchronize(dev)
 
+    mark("kv_heavy_budget512")
     # ---- where selected K/V bytes dominate: 16 requests of 65536 tokens at a
     # 512-page budget, the step over a bf16 and over an fp8 pool (each a CUDA
     # graph, timed back to back), and each sparse decode alone (L2 flushed).
@@ -480,6 +517,7 @@ def run_gpu(args):
     append_bytes = append_bytes_of(T)
     prefill_bytes = sum(append_bytes_of(c1 - c0) for c0, c1 in chunks)
 
+    mark("e2e")
     # ---- end to end through the public API: pinned host inputs in, results out
     # (a) The step's inputs (q, page table, lengths) and results (out, lse)
     # live in page-locked host memory and are passed to sv_quest_decode_step
@@ -537,6 +575,7 @@ def run_gpu(args):
                   and torch.equal(res_h[:out.numel() * 2].view(torch.bfloat16).view(out.shape).to(dev), out))
     h2d = sum(t.numel() * t.element_size() for t in (q_h, pt_h, sl_h))
     d2h = sum(t.numel() * t.element_size() for t in (out_h, lse_h))
+    mark.close()
 
     torch.cuda.synchronize(dev)
     flags = binding.sv_get_device_error(reset=True)
