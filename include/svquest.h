@@ -34,6 +34,10 @@
  *    call's inputs must not release its dependents early
  *    (griddepcontrol.launch_dependents): an ordinary kernel, a copy, or any
  *    work enqueued earlier is fine.
+ *  - The page metadata and the K/V tiles a call streams are read through an
+ *    L2 evict-first policy, so that they displace little else: what a call
+ *    reuses (page tables, scores, selections, split partials) and the
+ *    caller's other data tend to stay in L2 across calls.
  *  - Arguments are checked on the host before anything is launched.  A
  *    failed check returns a nonzero sv_status and launches nothing.  Values
  *    that live on the device (page tables, slot mappings, selected indices)
