@@ -7,6 +7,7 @@ builds from the command line; `-v` adds ptxas register/spill reports.
 """
 from __future__ import annotations
 
+import fcntl
 import glob
 import os
 import shutil
@@ -48,8 +49,18 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB_PATH
-    nvcc = _nvcc()
     os.makedirs(OUT_DIR, exist_ok=True)
+    # One build at a time: processes started together (one per GPU) share the
+    # object files; the ones that wait find the library built and return.
+    with open(os.path.join(OUT_DIR, ".build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and up_to_date():
+            return LIB_PATH
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose: bool) -> str:
+    nvcc = _nvcc()
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE,
                     "--expt-relaxed-constexpr"]
     if verbose:
