@@ -32,7 +32,12 @@ constexpr int kMaxSplits = 64;
 #ifndef SVQ_DECODE_WAVE_PERMILLE
 #define SVQ_DECODE_WAVE_PERMILLE 1000   // split CTAs as a fraction of one full wave
 #endif
-constexpr int kMinPagesPerSplit = 8;
+constexpr int kMinPagesPerSplit = 8;       // workspace bound: at most ceil(pages / 8) splits
+// Pages per split below which a split costs more (its setup, merge and partial,
+// and the combine's read of it) than its parallelism saves: the split count
+// is the smaller of one wave and pages / this (bf16 / e4m3 pools).
+constexpr int kSplitPagesBf16 = 24;
+constexpr int kSplitPagesFp8 = 16;
 // Online softmax with a lazily moved base: a head's running base moves only
 // when one of the page's logits exceeds it by more than this many log2 units.
 // Most pages then skip the warp max, the correction factors and the rescale
@@ -525,7 +530,8 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     if (c->kv_format == SV_KV_FP8_E4M3) {
         const bool per_head8 = per_q_head && sel_idx;
         const int rows8 = per_head8 ? num_q_heads : c->num_kv_heads;
-        const int splits8 = decode_fp8_splits(c, batch, rows8, pages, sm_count, decode_max_splits(pages));
+        const int cap8 = min(decode_max_splits(pages), (pages + kSplitPagesFp8 - 1) / kSplitPagesFp8);
+        const int splits8 = decode_fp8_splits(c, batch, rows8, pages, sm_count, cap8);
         if (splits8 < 1) return SV_ERR_CUDA;
         if (decode_workspace_bytes(batch, num_q_heads, splits8) > workspace_bytes) return SV_ERR_WORKSPACE;
         const size_t heads8 = static_cast<size_t>(batch) * num_q_heads * splits8;
@@ -553,7 +559,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     const int rows_per_req = per_head ? num_q_heads : c->num_kv_heads;
     const int bh = batch * rows_per_req;
     int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm * SVQ_DECODE_WAVE_PERMILLE / 1000) / bh);
-    splits = max(1, min(splits, decode_max_splits(pages)));
+    splits = max(1, min(splits, min(decode_max_splits(pages), (pages + kSplitPagesBf16 - 1) / kSplitPagesBf16)));
     if (decode_workspace_bytes(batch, num_q_heads, splits) > workspace_bytes) return SV_ERR_WORKSPACE;
 
     // TMA row coordinates are 32-bit.
