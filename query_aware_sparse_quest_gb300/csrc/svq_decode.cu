@@ -34,8 +34,8 @@ constexpr int kMaxSplits = 64;
 #endif
 constexpr int kMinPagesPerSplit = 8;       // workspace bound: at most ceil(pages / 8) splits
 // Pages per split below which a split costs more (its setup, merge and partial,
-// and the combine's read of it) than its parallelism saves: the split count
-// is the smaller of one wave and pages / this (bf16 / e4m3 pools).
+// and the combine's read of it) than its parallelism saves once the GPU is
+// full (bf16 / e4m3 pools).
 constexpr int kSplitPagesBf16 = 24;
 constexpr int kSplitPagesFp8 = 16;
 // Online softmax with a lazily moved base: a head's running base moves only
@@ -477,6 +477,15 @@ int decode_max_splits(int pages) {
     return max(1, min(kMaxSplits, cap));
 }
 
+// Most splits per row: rows of split_pages pages each when that many CTAs
+// still put one on every SM; otherwise (few rows) the finer bound, so that
+// idle SMs take the extra splits.
+int split_cap(int pages, int64_t rows, int sm_count, int split_pages) {
+    const int coarse = (pages + split_pages - 1) / split_pages;
+    const int fine = decode_max_splits(pages);
+    return static_cast<int64_t>(coarse) * rows >= sm_count ? max(1, min(fine, coarse)) : fine;
+}
+
 size_t decode_workspace_bytes(int batch, int num_q_heads, int splits) {
     const size_t heads = static_cast<size_t>(batch) * num_q_heads * splits;
     const size_t o_bytes = ((heads * kHeadDim * sizeof(float)) + 255) / 256 * 256;
@@ -530,7 +539,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     if (c->kv_format == SV_KV_FP8_E4M3) {
         const bool per_head8 = per_q_head && sel_idx;
         const int rows8 = per_head8 ? num_q_heads : c->num_kv_heads;
-        const int cap8 = min(decode_max_splits(pages), (pages + kSplitPagesFp8 - 1) / kSplitPagesFp8);
+        const int cap8 = split_cap(pages, static_cast<int64_t>(batch) * rows8, sm_count, kSplitPagesFp8);
         const int splits8 = decode_fp8_splits(c, batch, rows8, pages, sm_count, cap8);
         if (splits8 < 1) return SV_ERR_CUDA;
         if (decode_workspace_bytes(batch, num_q_heads, splits8) > workspace_bytes) return SV_ERR_WORKSPACE;
@@ -559,7 +568,7 @@ int launch_decode(const sv_cache* c, const void* q, int num_q_heads, const int32
     const int rows_per_req = per_head ? num_q_heads : c->num_kv_heads;
     const int bh = batch * rows_per_req;
     int splits = static_cast<int>((static_cast<int64_t>(sm_count) * per_sm * SVQ_DECODE_WAVE_PERMILLE / 1000) / bh);
-    splits = max(1, min(splits, min(decode_max_splits(pages), (pages + kSplitPagesBf16 - 1) / kSplitPagesBf16)));
+    splits = max(1, min(splits, split_cap(pages, bh, sm_count, kSplitPagesBf16)));
     if (decode_workspace_bytes(batch, num_q_heads, splits) > workspace_bytes) return SV_ERR_WORKSPACE;
 
     // TMA row coordinates are 32-bit.
