@@ -1,7 +1,8 @@
-"""The benchmark's byte accounting (the roofline numerator), checked against
-counts written out by hand from the layouts: per (page, kv head) 512 bytes of
-metadata and 2 x 16 x 128 bf16 of K/V, 4 bytes of page table per page, q read
-once and out / lse written once."""
+"""The benchmark's host logic: its byte accounting (the roofline numerator),
+checked against counts written out by hand from the layouts (per (page, kv
+head) 512 bytes of metadata and 2 x 16 x 128 bf16 of K/V, 4 bytes of page
+table per page, q read once and out / lse written once); the rule that drops
+a profile's ncu traffic once its kernel source changes; the NVTX sections."""
 from __future__ import annotations
 
 import numpy as np
@@ -55,3 +56,42 @@ def test_step_bytes_count_the_appended_token():
               + s.batch * s.num_kv_heads * 128 * 2 * 4 + s.batch * s.num_kv_heads * 2 * 128 * 2)
     assert with_append - base == expect
     assert np.all(wl.seq_lens == 16 * 30)
+
+
+def test_kernel_traffic_is_dropped_once_the_source_changes(tmp_path, monkeypatch):
+    """The ncu traffic of a committed profile is reported only while the
+    kernel's source still hashes to the value stored beside it."""
+    import hashlib
+    src = tmp_path / "kernel.cu"
+    src.write_text("__global__ void k() {}\n")
+    digest = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    prof = tmp_path / "k.txt"
+    prof.write_text("# summary\nk.source_sha256_16=%s\nk.dram_bytes_per_launch_full_size=123456\n" % digest)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setitem(bench.PROFILE_SUMMARIES, "k", "k.txt")
+    monkeypatch.setitem(bench.KERNEL_SOURCES, "k", "kernel.cu")
+    assert bench.kernel_traffic("k") == 123456.0
+    src.write_text("__global__ void k() { }\n")   # any edit of the source
+    assert bench.kernel_traffic("k") is None
+
+
+def test_sections_open_and_close_nvtx_ranges_in_pairs(monkeypatch):
+    calls = []
+
+    class FakeNvtx:
+        @staticmethod
+        def range_push(name):
+            calls.append(("push", name))
+
+        @staticmethod
+        def range_pop():
+            calls.append(("pop",))
+
+    monkeypatch.setattr(bench.torch.cuda, "nvtx", FakeNvtx)
+    mark = bench.Sections()
+    calls.clear()
+    mark("a")
+    mark("b")
+    mark.close()
+    mark.close()
+    assert calls == [("push", "a"), ("pop",), ("push", "b"), ("pop",)]
