@@ -88,9 +88,22 @@ def _load():
     return lib
 
 
-def _p(t: Optional[torch.Tensor]):
+_BF16, _I32, _F32 = torch.bfloat16, torch.int32, torch.float32
+
+
+def _p(t: Optional[torch.Tensor], dtype: Optional[torch.dtype] = None, name: str = "tensor",
+       host_ok: bool = False):
+    """The tensor's address for the C ABI, after checking what the kernels
+    assume of it: contiguous, of the given dtype, in device memory (or, where
+    host_ok, in page-locked host memory)."""
     if t is None:
         return None
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda and not (host_ok and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor" + (" or page-locked host memory" if host_ok else ""))
     return ctypes.c_void_p(t.data_ptr())
 
 
@@ -117,6 +130,15 @@ class Cache:
         self.k_scale, self.v_scale = k_scale, v_scale
         n, hkv, p, d = k_pool.shape
         fp8 = k_pool.dtype == torch.uint8
+        pool_t = torch.uint8 if fp8 else _BF16
+        _p(k_pool, pool_t, "k_pool")
+        _p(v_pool, pool_t, "v_pool")
+        _p(meta, _BF16, "meta")
+        if fp8:
+            if k_scale is None or v_scale is None:
+                raise ValueError("an e4m3 pool needs k_scale and v_scale")
+            _p(k_scale, _F32, "k_scale")
+            _p(v_scale, _F32, "v_scale")
         self.c = sv_cache(k_pool.data_ptr(), v_pool.data_ptr(), meta.data_ptr(), n, hkv, p, d,
                           SV_KV_FP8_E4M3 if fp8 else SV_KV_BF16,
                           k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None)
@@ -141,22 +163,24 @@ class Cache:
 def sv_quest_update_meta(cache: Cache, k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
                          stream=None) -> None:
     _check("sv_quest_update_meta", _load().sv_quest_update_meta(
-        cache.ref(), _p(k_new), _p(v_new), _p(slot_mapping), int(slot_mapping.numel()), _stream(stream)))
+        cache.ref(), _p(k_new, _BF16, "k_new"), _p(v_new, _BF16, "v_new"), _p(slot_mapping, _I32, "slot_mapping"),
+        int(slot_mapping.numel()), _stream(stream)))
 
 
 def sv_quest_score(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq_lens: torch.Tensor,
                    scores: torch.Tensor, stream=None) -> None:
     B, Hq, _ = q.shape
     _check("sv_quest_score", _load().sv_quest_score(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(scores),
-        _stream(stream)))
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), _p(scores, _F32, "scores"), _stream(stream)))
 
 
 def sv_quest_topk(scores: torch.Tensor, seq_lens: torch.Tensor, budget_pages: int, sel_idx: torch.Tensor,
                   sel_cnt: torch.Tensor, stream=None) -> None:
     B, Hkv, max_pages = scores.shape
     _check("sv_quest_topk", _load().sv_quest_topk(
-        _p(scores), _p(seq_lens), B, Hkv, max_pages, int(budget_pages), _p(sel_idx), _p(sel_cnt), _stream(stream)))
+        _p(scores, _F32, "scores"), _p(seq_lens, _I32, "seq_lens"), B, Hkv, max_pages, int(budget_pages),
+        _p(sel_idx, _I32, "sel_idx"), _p(sel_cnt, _I32, "sel_cnt"), _stream(stream)))
 
 
 def sv_quest_select_workspace_size(batch: int, num_kv_heads: int, max_pages: int) -> int:
@@ -170,8 +194,10 @@ def sv_quest_select(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, seq
     B, Hq, _ = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("sv_quest_select", _load().sv_quest_select(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
-        _p(sel_idx), _p(sel_cnt), _p(scores_out), _p(workspace), ws_bytes, _stream(stream)))
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), int(budget_pages),
+        _p(sel_idx, _I32, "sel_idx"), _p(sel_cnt, _I32, "sel_cnt"), _p(scores_out, _F32, "scores_out"),
+        _p(workspace, None, "workspace"), ws_bytes, _stream(stream)))
 
 
 def sv_sparse_decode_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, pages: int) -> int:
@@ -186,8 +212,10 @@ def sv_sparse_decode(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, se
     K = 0 if sel_idx is None else int(sel_idx.shape[2])
     scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
     _check("sv_sparse_decode", _load().sv_sparse_decode(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
-        _p(sel_cnt), K, scale, _p(out), _p(lse), _p(workspace), workspace.numel() * workspace.element_size(),
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), _p(sel_idx, _I32, "sel_idx"),
+        _p(sel_cnt, _I32, "sel_cnt"), K, scale, _p(out, _BF16, "out"), _p(lse, _F32, "lse"),
+        _p(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)))
 
 
@@ -200,8 +228,9 @@ def sv_sparse_decode_static_scratch(cache: Cache, q: torch.Tensor, page_table: t
     K = 0 if sel_idx is None else int(sel_idx.shape[2])
     scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
     _check("sv_sparse_decode_static_scratch", _load().sv_sparse_decode_static_scratch(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
-        _p(sel_cnt), K, scale, _p(out), _p(lse), _stream(stream)))
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), _p(sel_idx, _I32, "sel_idx"),
+        _p(sel_cnt, _I32, "sel_cnt"), K, scale, _p(out, _BF16, "out"), _p(lse, _F32, "lse"), _stream(stream)))
 
 
 def sv_quest_decode_step_workspace_size(batch: int, num_q_heads: int, num_kv_heads: int, max_pages: int,
@@ -215,8 +244,10 @@ def _step(name: str, cache: Cache, q, page_table, seq_lens, budget_pages, sel_id
     B, Hq, D = q.shape
     scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
     _check(name, getattr(_load(), name)(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
-        scale, _p(sel_idx), _p(sel_cnt), _p(out), _p(lse), _p(workspace),
+        cache.ref(), _p(q, _BF16, "q", True), Hq, _p(page_table, _I32, "page_table", True),
+        _p(seq_lens, _I32, "seq_lens", True), B, int(page_table.shape[1]), int(budget_pages), scale,
+        _p(sel_idx, _I32, "sel_idx"), _p(sel_cnt, _I32, "sel_cnt"), _p(out, _BF16, "out", True),
+        _p(lse, _F32, "lse", True), _p(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -246,8 +277,10 @@ def sv_quest_select_ex(cache: Cache, q: torch.Tensor, page_table: torch.Tensor, 
     B, Hq, _ = q.shape
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check("sv_quest_select_ex", _load().sv_quest_select_ex(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), int(budget_pages),
-        None if opts is None else ctypes.byref(opts), _p(sel_idx), _p(sel_cnt), _p(scores_out), _p(workspace),
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), int(budget_pages),
+        None if opts is None else ctypes.byref(opts), _p(sel_idx, _I32, "sel_idx"), _p(sel_cnt, _I32, "sel_cnt"), _p(scores_out, _F32, "scores_out"),
+        _p(workspace, None, "workspace"),
         ws_bytes, _stream(stream)))
 
 
@@ -259,8 +292,10 @@ def sv_sparse_decode_ex(cache: Cache, q: torch.Tensor, page_table: torch.Tensor,
     K = 0 if sel_idx is None else int(sel_idx.shape[2])
     scale = float(D) ** -0.5 if softmax_scale is None else float(softmax_scale)
     _check("sv_sparse_decode_ex", _load().sv_sparse_decode_ex(
-        cache.ref(), _p(q), Hq, _p(page_table), _p(seq_lens), B, int(page_table.shape[1]), _p(sel_idx),
-        _p(sel_cnt), K, None if opts is None else ctypes.byref(opts), scale, _p(out), _p(lse), _p(workspace),
+        cache.ref(), _p(q, _BF16, "q"), Hq, _p(page_table, _I32, "page_table"), _p(seq_lens, _I32, "seq_lens"), B,
+        int(page_table.shape[1]), _p(sel_idx, _I32, "sel_idx"),
+        _p(sel_cnt, _I32, "sel_cnt"), K, None if opts is None else ctypes.byref(opts), scale,
+        _p(out, _BF16, "out"), _p(lse, _F32, "lse"), _p(workspace, None, "workspace"),
         workspace.numel() * workspace.element_size(), _stream(stream)))
 
 

@@ -228,3 +228,25 @@ def test_fp8_cache_checks(lib):
     assert sel(cache(binding.SV_KV_FP8_E4M3, vs=0x10004)) == SV_ERR_INVALID_ARG  # 16-byte aligned
     assert sel(cache(7)) == SV_ERR_UNSUPPORTED
     assert ctypes.sizeof(binding.sv_cache) == 64
+
+
+def test_binding_rejects_tensors_the_kernels_cannot_take():
+    """Argument marshalling: a tensor reaches the C ABI only if it is
+    contiguous, of the dtype the kernels read, and in device memory (or, for
+    the one-call step's per-step buffers, page-locked host memory)."""
+    import pytest
+    import torch
+    t = torch.zeros(4, 8, dtype=torch.int32)
+    assert binding._p(None) is None
+    with pytest.raises(ValueError, match="contiguous"):
+        binding._p(t.t(), torch.int32, "page_table")
+    with pytest.raises(TypeError, match="seq_lens"):
+        binding._p(t.long(), torch.int32, "seq_lens")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        binding._p(t, torch.int32, "page_table")
+    with pytest.raises(ValueError, match="page-locked"):
+        binding._p(t, torch.int32, "page_table", host_ok=True)
+    pool = torch.zeros(2, 1, 16, 128, dtype=torch.bfloat16)
+    meta = torch.zeros(2, 1, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="k_pool"):
+        binding.Cache(pool, pool, meta)
