@@ -146,3 +146,34 @@ def test_dense_layers_skip_selection():
     # The layer after the dense ones selects normally.
     opts2 = binding.quest_opts(layer=3, dense_layers=3)
     check_variant(host, wl, 9, opts2, run_variant(dw, 9, opts2))
+
+
+@pytest.mark.parametrize("per_q_head,sink,window", [(True, 0, 0), (False, 1, 4)])
+def test_variant_parity_at_full_size_sampled(per_q_head, sink, window):
+    """The options on the 128k batch-8 workload (8000 pages per request, 256-page
+    budget, shuffled pool), as the benchmark runs them; sampled requests are
+    checked against the oracle one by one."""
+    from test_gpu_parity import pair
+    pr = pair(2)
+    wl, host, K = pr.wl, pr.host, pr.wl.spec.budget_pages
+    opts = binding.quest_opts(per_q_head=per_q_head, sink_pages=sink, window_pages=window)
+    sel, cnt, scores, out, lse = run_variant(pr.dw, K, opts)
+    n_all = n_pages_of(wl)
+    for b in (0, 5):
+        sl = slice(b, b + 1)
+        nb = int(n_all[b])
+        ref_sel, ref_cnt, ref_scores = oracle.select(host, wl.q[sl], wl.page_table[sl], wl.seq_lens[sl], K,
+                                                     per_q_head=per_q_head, sink_pages=sink, window_pages=window)
+        forced = np.zeros(nb, bool)
+        forced[: min(nb, sink)] = True
+        if window:
+            forced[max(0, nb - window):] = True
+        ranked = ref_scores.copy()
+        ranked[0, :, :nb][:, forced] = np.inf
+        gpu = scores[b, :, :nb]
+        assert np.all(np.isinf(gpu[:, forced]) & (gpu[:, forced] > 0))
+        r = ref_scores[0, :, :nb][:, ~forced].astype(np.float64)
+        np.testing.assert_allclose(gpu[:, ~forced], r, rtol=1e-5, atol=1e-5 * np.abs(r).max())
+        check_selection(sel[sl], cnt[sl], ref_sel, ref_cnt, ranked, n_all[sl])
+        check_attention(out[sl], lse[sl], *oracle.decode(host, wl.q[sl], wl.page_table[sl], wl.seq_lens[sl],
+                                                         sel[sl], cnt[sl], per_q_head=per_q_head))
