@@ -184,3 +184,28 @@ def test_fp8_step_full_size_128k():
         ref_out, ref_lse = oracle.decode(host, wl.q[rows], wl.page_table[rows], wl.seq_lens[rows], sel[rows],
                                          cnt[rows])
         check_attention(out[rows], lse[rows], ref_out, ref_lse)
+
+
+def test_fp8_step_full_size_512_page_budget():
+    """The workload where selected K/V dominate (16 requests of 65536 tokens
+    plus one appended slot, 512-page budget, shuffled pool) on an fp8 pool
+    through sv_quest_decode_step: every selection against the oracle, attention
+    of sampled requests against the oracle's fp8 decode over those selections."""
+    wl, dw, host = _pair(synth.SPECS[4].scaled(budget_pages=512))
+    spec = wl.spec
+    K = 512
+    B, Hq, D = dw.q.shape
+    ws = resident.workspace(binding.sv_quest_decode_step_workspace_size(B, Hq, spec.num_kv_heads, wl.max_pages, K))
+    sel_idx, sel_cnt = resident.select_buffers(B, spec.num_kv_heads, K)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    binding.sv_quest_decode_step(dw.cache, dw.q, dw.page_table, dw.seq_lens, K, sel_idx, sel_cnt, out, lse, ws)
+    sel, cnt = sel_idx.cpu().numpy(), sel_cnt.cpu().numpy()
+    out, lse = out.float().cpu().numpy(), lse.cpu().numpy()
+    ref_sel, ref_cnt, ref_scores = oracle.select(host, wl.q, wl.page_table, wl.seq_lens, K)
+    check_selection(sel, cnt, ref_sel, ref_cnt, ref_scores, n_pages_of(wl))
+    for b in (0, 9, 15):
+        rows = slice(b, b + 1)
+        ref_out, ref_lse = oracle.decode(host, wl.q[rows], wl.page_table[rows], wl.seq_lens[rows], sel[rows],
+                                         cnt[rows])
+        check_attention(out[rows], lse[rows], ref_out, ref_lse)
